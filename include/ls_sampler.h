@@ -1,0 +1,163 @@
+/*
+ * ls_sampler.h -- C ABI of the GB300 token sampler (libls_sampler.so).
+ *
+ * The library samples one token id per row of a [rows, vocab] logits matrix
+ * and computes the per-row log-probs of the processed distribution
+ * (temperature, exact top-k, exact top-p).  Every call is asynchronous on the
+ * caller's CUDA stream, allocates nothing, never synchronises with the host
+ * and launches one kernel.
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ * - Pointers: every buffer argument is a DEVICE pointer (cudaMalloc /
+ *   cudaMallocManaged / a device view of pinned host memory) owned by the
+ *   caller, except `params`, which points to a small HOST struct whose fields
+ *   are device pointers.  Results are valid once `stream` has reached the
+ *   call's completion.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ * - Layout: logits row r starts at element r * row_stride; vocab <= row_stride.
+ *   Rows need no particular alignment.
+ * - Sampling parameters (struct ls_params) are indexed by request; row i uses
+ *   request token_to_request_index[i] when that array is given, else request i.
+ *     temperature  T < 1e-5 (or NaN) -> greedy row: the id is the lowest index
+ *                  of the row maximum, no noise.
+ *     top_k        k <= 0 or k >= vocab -> top-k off for that row.  Kept set:
+ *                  entries >= the k-th largest logit (ties at the cut kept).
+ *     top_p        p >= 0.99999 (or NaN) -> top-p off.  Kept set: walking the
+ *                  distinct values downwards, the first value at which the
+ *                  cumulative probability reaches p; everything at or above it
+ *                  is kept.  p <= 0 keeps the maximum and its ties.
+ *     seed         Philox4x32-10 key (lo32, hi32) of the request.
+ *   Joint filtering applies top-k first, then top-p on the renormalised top-k
+ *   distribution.
+ * - Noise: entry j of output row i at step s gets the word (j mod 4) of
+ *   Philox4x32-10(counter = (j/4, i, lo32 s, hi32 s), key = seed), mapped to
+ *   u = (2*(x>>9)+1) * 2^-24 and g = -ln(-ln u).  The id is the argmax of
+ *   z_j + g_j over the kept set (z = logit / T), lowest index on an exact tie.
+ *   The same (seed, step, row) always gives the same id; a new step gives
+ *   fresh noise.
+ * - Special values: NaN logits are read as -inf; -inf entries are never kept.
+ *   A row whose maximum is +inf samples uniformly among its +inf entries.
+ * - Errors found on the host (bad arguments) return a status before any launch.
+ *   Errors found per row on the device (index out of range, a row with no
+ *   entry above -inf) write id -1 (log-probs NaN) for that row and OR a bit
+ *   into *error_word when error_word is not NULL:
+ *     LS_ROW_ERR_BAD_GATHER  gather_indices[i] outside [0, logits_rows)
+ *     LS_ROW_ERR_BAD_REQUEST request index outside [0, params->num_requests)
+ *     LS_ROW_ERR_NO_FINITE   every entry of the row is -inf or NaN
+ *   The library never clears *error_word.
+ */
+#ifndef LS_SAMPLER_H
+#define LS_SAMPLER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LS_OK = 0,
+  LS_ERR_INVALID_ARG = 1, /* a host-checkable argument is wrong; nothing launched */
+  LS_ERR_UNSUPPORTED = 2, /* valid but beyond this build's limits (e.g. vocab too large) */
+  LS_ERR_CUDA = 3         /* the launch failed; cudaGetLastError() holds the reason */
+} ls_status;
+
+typedef enum { LS_DTYPE_F32 = 0, LS_DTYPE_BF16 = 1 } ls_dtype;
+
+enum { LS_ROW_ERR_BAD_GATHER = 1, LS_ROW_ERR_BAD_REQUEST = 2, LS_ROW_ERR_NO_FINITE = 4 };
+
+/* Per-request sampling parameters: device arrays of length num_requests, owned
+ * by the caller (the per-request sampling metadata a serving controller keeps
+ * on the GPU). */
+typedef struct {
+  const float* temperature;
+  const int32_t* top_k;
+  const float* top_p;
+  const uint64_t* seed;
+  int32_t num_requests;
+} ls_params;
+
+/*
+ * ls_sample -- sample n token ids.
+ *
+ * Follows "core.inference.sampling.base" (Sampling.sample_kernel) and
+ * "core.inference.sampling.flashinfer_sampling" (FlashInferSampling.
+ * sample_kernel): sample n tokens from logits[>= n, vocab]; with
+ * gather_indices, row i reads logits[gather_indices[i]]; with
+ * token_to_request_index, parameters are gathered per token.  The batch flags
+ * no_top_k / no_top_p (computed by the caller from host-side metadata) pick
+ * the route -- no filter, top-k only, top-p only or joint -- with no device
+ * read and no sync.  A set flag switches that filter off for every row.
+ *
+ *   logits          device, dtype elements, logits_rows x row_stride
+ *   logits_rows     rows addressable in logits (>= n when gather_indices is NULL)
+ *   vocab           entries per row, 1 <= vocab <= row_stride
+ *   n               rows to sample, >= 0 (0: nothing launched, LS_OK)
+ *   gather_indices  device int32[n] or NULL
+ *   token_to_request_index  device int32[n] or NULL (NULL: row i -> request i)
+ *   params          host pointer to device parameter arrays
+ *   step            Philox step word (advance it every decoding step)
+ *   out_ids         device int32[n], written by the call
+ *   error_word      device int32 or NULL
+ *   stream          cudaStream_t
+ */
+ls_status ls_sample(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                    int32_t n, const int32_t* gather_indices, const int32_t* token_to_request_index,
+                    const ls_params* params, uint64_t step, int no_top_k, int no_top_p, int32_t* out_ids,
+                    int32_t* error_word, void* stream);
+
+/*
+ * ls_sample_speculative -- sample the speculative-verify rows.
+ *
+ * Follows "core.inference.sampling.base" (Sampling.sample_speculative): decode
+ * requests contribute 1 + num_speculative_tokens rows and prefill requests 1,
+ * so n = num_decode * (1 + S) + num_prefill.  Row r belongs to request
+ * r / (1 + S) when r < num_decode * (1 + S), else to request
+ * num_decode + (r - num_decode * (1 + S)) (decode rows first).  With
+ * gather_indices, row r reads logits[gather_indices[r]]; without, logits are
+ * already in that layout (logits_rows >= n).  Requires
+ * params->num_requests >= num_decode + num_prefill.
+ *
+ *   out_ids                       device int32[n]
+ *   out_token_to_request_index    device int32[n] or NULL: the mapping above
+ * Other arguments as for ls_sample.
+ */
+ls_status ls_sample_speculative(const void* required_logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
+                                int64_t row_stride, int32_t num_decode, int32_t num_prefill,
+                                int32_t num_speculative_tokens, const int32_t* gather_indices,
+                                const ls_params* params, uint64_t step, int no_top_k, int no_top_p,
+                                int32_t* out_ids, int32_t* out_token_to_request_index, int32_t* error_word,
+                                void* stream);
+
+/*
+ * ls_log_probs -- per-row log-probs of the processed distribution.
+ *
+ * Follows "core.inference.sampling.flashinfer_sampling" (FlashInferSampling.
+ * log_probs_kernel): raw logits [num_rows, vocab], optional row -> request
+ * mapping; output = log-probs of the distribution the sampler draws from
+ * (every row's own temperature, top-k and top-p; no route flags).
+ * out[i, j] = z_j - max_K z - ln sum_K exp(z - max_K z) for j in the kept set
+ * K, -inf elsewhere (z = logit / T; greedy rows: -ln(#ties) on the maximum's
+ * ties).  gather_indices is an extension the page does not have (NULL: row i
+ * reads logits row i).
+ *
+ *   out_log_probs   device float[num_rows * vocab], row-major, written fully
+ * Other arguments as for ls_sample.
+ */
+ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                       int32_t num_rows, const int32_t* gather_indices, const int32_t* token_to_request_index,
+                       const ls_params* params, float* out_log_probs, int32_t* error_word, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* ls_status_string(ls_status s);
+
+/* Largest vocab the kernels accept for a dtype on the current device (shared
+ * memory bound), or 0 when no CUDA device is available. */
+int64_t ls_max_vocab(ls_dtype dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LS_SAMPLER_H */

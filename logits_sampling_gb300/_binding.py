@@ -1,0 +1,203 @@
+"""ctypes binding of include/ls_sampler.h (argument marshalling only)."""
+import ctypes
+import os
+from dataclasses import dataclass
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libls_sampler.so"
+
+LS_OK, LS_ERR_INVALID_ARG, LS_ERR_UNSUPPORTED, LS_ERR_CUDA = 0, 1, 2, 3
+LS_DTYPE_F32, LS_DTYPE_BF16 = 0, 1
+LS_ROW_ERR_BAD_GATHER, LS_ROW_ERR_BAD_REQUEST, LS_ROW_ERR_NO_FINITE = 1, 2, 4
+
+_lib = None
+
+
+class LSError(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__(f"{what}: {status_string(status)}")
+        self.status = status
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_void_p), ("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p),
+                ("seed", ctypes.c_void_p), ("num_requests", ctypes.c_int32)]
+
+
+def lib_path():
+    return os.path.join(PKG, LIB_NAME)
+
+
+def load_library():
+    """Load libls_sampler.so from the package directory (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m logits_sampling_gb300.build` "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, u64, ci = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
+    PP = ctypes.POINTER(_Params)
+    lib.ls_sample.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P]
+    lib.ls_sample.restype = ci
+    lib.ls_sample_speculative.argtypes = [P, ci, i64, i64, i64, i32, i32, i32, P, PP, u64, ci, ci, P, P, P, P]
+    lib.ls_sample_speculative.restype = ci
+    lib.ls_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, P, P]
+    lib.ls_log_probs.restype = ci
+    lib.ls_status_string.argtypes = [ci]
+    lib.ls_status_string.restype = ctypes.c_char_p
+    lib.ls_max_vocab.argtypes = [ci]
+    lib.ls_max_vocab.restype = i64
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    try:
+        return load_library().ls_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover
+        return f"status {status}"
+
+
+def max_vocab(dtype=LS_DTYPE_BF16):
+    return int(load_library().ls_max_vocab(dtype))
+
+
+@dataclass
+class SamplingParams:
+    """Per-request parameters as device tensors (float32 temperature, int32
+    top_k, float32 top_p, int64/uint64 seed), all of length num_requests."""
+    temperature: object
+    top_k: object
+    top_p: object
+    seed: object = None
+
+    def as_struct(self):
+        n = int(self.temperature.numel())
+        for name in ("top_k", "top_p", "seed"):
+            t = getattr(self, name)
+            if t is not None and int(t.numel()) != n:
+                raise ValueError(f"{name} has {t.numel()} entries, temperature has {n}")
+        import torch
+        if self.temperature.dtype != torch.float32 or self.top_p.dtype != torch.float32:
+            raise TypeError("temperature and top_p must be float32")
+        if self.top_k.dtype != torch.int32:
+            raise TypeError("top_k must be int32")
+        if self.seed is not None and self.seed.dtype not in (torch.int64, torch.uint64):
+            raise TypeError("seed must be int64 or uint64")
+        return _Params(_dptr(self.temperature), _dptr(self.top_k), _dptr(self.top_p),
+                       _dptr(self.seed) if self.seed is not None else None, n)
+
+    @staticmethod
+    def from_host(temperature, top_k, top_p, seed, device="cuda"):
+        import numpy as np
+        import torch
+        return SamplingParams(
+            torch.from_numpy(np.ascontiguousarray(temperature, np.float32)).to(device),
+            torch.from_numpy(np.ascontiguousarray(top_k, np.int32)).to(device),
+            torch.from_numpy(np.ascontiguousarray(top_p, np.float32)).to(device),
+            torch.from_numpy(np.ascontiguousarray(seed, np.uint64).view(np.int64)).to(device))
+
+
+def _dptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _logits_desc(logits):
+    import torch
+    if logits.dim() != 2:
+        raise ValueError("logits must be 2-D [rows, vocab]")
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous (stride(1) == 1)")
+    if logits.dtype == torch.float32:
+        dt = LS_DTYPE_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = LS_DTYPE_BF16
+    else:
+        raise TypeError(f"unsupported logits dtype {logits.dtype}")
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor")
+    return ctypes.c_void_p(logits.data_ptr()), dt, logits.shape[0], logits.shape[1], logits.stride(0)
+
+
+def _i32(t, what):
+    import torch
+    if t is None:
+        return None
+    if t.dtype != torch.int32:
+        raise TypeError(f"{what} must be int32")
+    return _dptr(t)
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def sample(logits, n, params, step, no_top_k, no_top_p, gather_indices=None, token_to_request_index=None,
+           out=None, error_word=None, stream=None):
+    """ls_sample: returns out (int32 [n] on the logits' device)."""
+    import torch
+    lib = load_library()
+    ptr, dt, rows, V, stride = _logits_desc(logits)
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=logits.device)
+    prm = params.as_struct()
+    st = lib.ls_sample(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
+                       _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm), int(step),
+                       int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"), _i32(error_word, "error_word"),
+                       _stream(stream))
+    if st != LS_OK:
+        raise LSError(st, "ls_sample")
+    return out
+
+
+def sample_speculative(required_logits, num_decode, num_prefill, num_speculative_tokens, params, step, no_top_k,
+                       no_top_p, gather_indices=None, out=None, out_token_to_request_index=None, error_word=None,
+                       stream=None):
+    """ls_sample_speculative: returns out (int32 [num_decode*(1+S)+num_prefill])."""
+    import torch
+    lib = load_library()
+    ptr, dt, rows, V, stride = _logits_desc(required_logits)
+    n = num_decode * (1 + num_speculative_tokens) + num_prefill
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=required_logits.device)
+    prm = params.as_struct()
+    st = lib.ls_sample_speculative(ptr, dt, rows, V, stride, int(num_decode), int(num_prefill),
+                                   int(num_speculative_tokens), _i32(gather_indices, "gather_indices"),
+                                   ctypes.byref(prm), int(step), int(bool(no_top_k)), int(bool(no_top_p)),
+                                   _i32(out, "out"), _i32(out_token_to_request_index, "out_token_to_request_index"),
+                                   _i32(error_word, "error_word"), _stream(stream))
+    if st != LS_OK:
+        raise LSError(st, "ls_sample_speculative")
+    return out
+
+
+def log_probs(logits, params, num_rows=None, gather_indices=None, token_to_request_index=None, out=None,
+              error_word=None, stream=None):
+    """ls_log_probs: returns out (float32 [num_rows, vocab])."""
+    import torch
+    lib = load_library()
+    ptr, dt, rows, V, stride = _logits_desc(logits)
+    if num_rows is None:
+        num_rows = len(gather_indices) if gather_indices is not None else rows
+    if out is None:
+        out = torch.empty((num_rows, V), dtype=torch.float32, device=logits.device)
+    if out.dtype != torch.float32 or not out.is_contiguous() or out.numel() < num_rows * V:
+        raise ValueError("out must be a contiguous float32 tensor of num_rows * vocab entries")
+    prm = params.as_struct()
+    st = lib.ls_log_probs(ptr, dt, rows, V, stride, int(num_rows), _i32(gather_indices, "gather_indices"),
+                          _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
+                          _dptr(out), _i32(error_word, "error_word"), _stream(stream))
+    if st != LS_OK:
+        raise LSError(st, "ls_log_probs")
+    return out

@@ -1,0 +1,744 @@
+// ls_sampler.cu -- GB300 (sm_103a) kernels and C ABI of the token sampler.
+//
+// One CTA of 512 threads owns one sampled row.  The row is read from HBM once,
+// with 256-bit loads, by a single streaming pass that keeps, per group of 16
+// logits, the group maximum in shared memory and, per thread, a running
+// maximum and (when the row needs it) the online sum of exp((l - max) / T).
+// Everything after that pass touches only candidate groups -- groups whose
+// maximum clears a provable lower bound of what can be kept or sampled -- and
+// re-reads them from L2:
+//   * exact top-k cut: an adaptive 11-bit radix select on order-preserving keys;
+//   * exact top-p cut: the same select weighted by fixed-point masses
+//     (deterministic 64-bit integer atomics), joint = top-k cut first;
+//   * Gumbel-max over the kept set with in-register Philox4x32-10 noise, only
+//     for entries within the noise span of the row maximum.
+// The log-probs kernel runs the same selection and then writes the full
+// [vocab] row of log-probs.
+//
+// The behaviour follows "core.inference.sampling.base" (Sampling.sample_kernel,
+// Sampling.sample_speculative), "core.inference.sampling.flashinfer_sampling"
+// (FlashInferSampling: per-step top-p-only / top-k-only / joint dispatch from
+// host flags, log_probs_kernel) and the TokenSpeed "backends/triton.py" page
+// (TritonSamplingBackend: Gumbel-max sampling from per-request pools).
+
+#include <cfloat>
+#include <cstdint>
+#include <cstdio>
+#include <cuda_runtime.h>
+
+#include "ls_device.cuh"
+#include "ls_sampler.h"
+
+namespace lsg {
+
+enum MapMode { MAP_IDENTITY = 0, MAP_T2R = 1, MAP_SPEC = 2 };
+enum Mode { MODE_SAMPLE = 0, MODE_LOGPROBS = 1 };
+enum Route { ROUTE_NONE = 0, ROUTE_K = 1, ROUTE_P = 2, ROUTE_KP = 3 };
+
+struct KernelArgs {
+  const void* logits;
+  int64_t logits_rows, vocab, stride;
+  const int32_t* gather;
+  const int32_t* t2r;
+  int map_mode;
+  int32_t spec_decode_rows;  // num_decode * (1 + S)
+  int32_t spec_per_req;      // 1 + S
+  int32_t spec_num_decode;
+  const float* temperature;
+  const int32_t* top_k;
+  const float* top_p;
+  const uint64_t* seed;
+  int32_t num_requests;
+  uint64_t step;
+  int32_t* out_ids;
+  int32_t* out_t2r;
+  float* out_lp;
+  int32_t* error_word;
+};
+
+// Fixed part of the dynamic shared memory; the group maxima follow it.
+struct Shared {
+  unsigned long long hist[kBins];
+  unsigned long long red_u64[kWarps];
+  float red_f[kWarps];
+  int red_i[kWarps];
+  unsigned long long best;
+  unsigned long long acc;
+  unsigned long long cut_above;
+  unsigned long long cut_mass;
+  int cut_bin;
+  int min_index;
+};
+
+// ---------------------------------------------------------------------------
+// Row view: groups of 16 logits aligned to the group size in bytes, so that
+// every interior group is one (bf16) or two (fp32) aligned 256-bit loads.
+// Group g covers row entries [16 g - off, 16 g - off + 16); entries outside
+// [0, vocab) read as -inf.
+// ---------------------------------------------------------------------------
+template <typename TIn>
+struct RowView;
+
+__device__ __forceinline__ void ld256(const void* p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+template <>
+struct RowView<bf16_tag> {
+  static constexpr int kBytes = 2;
+  const uint16_t* row;
+  const unsigned char* base;  // group 0, aligned to 32 bytes
+  int off;
+  int64_t V;
+  int NG;
+  __device__ __forceinline__ void init(const void* logits, int64_t src, int64_t stride, int64_t vocab) {
+    row = static_cast<const uint16_t*>(logits) + src * stride;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    base = reinterpret_cast<const unsigned char*>(a & ~uintptr_t(31));
+    off = (int)((a - reinterpret_cast<uintptr_t>(base)) / 2);
+    V = vocab;
+    NG = (int)((off + vocab + kGroup - 1) / kGroup);
+  }
+  __device__ __forceinline__ int64_t index(int g, int e) const { return (int64_t)g * kGroup - off + e; }
+  static constexpr int kWords = 8;
+  __device__ __forceinline__ float at(int64_t j) const { return bf16_bits_to_float(row[j]); }
+  __device__ __forceinline__ bool full(int g) const {
+    const int64_t j0 = index(g, 0);
+    return j0 >= 0 && j0 + kGroup <= V;
+  }
+  __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords]) const { ld256(base + (size_t)g * 32, w); }
+  __device__ __forceinline__ static void unpack(const uint32_t (&w)[kWords], float (&v)[kGroup]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  }
+  __device__ __forceinline__ void load(int g, float (&v)[kGroup]) const {
+    const int64_t j0 = index(g, 0);
+    if (j0 >= 0 && j0 + kGroup <= V) {
+      uint32_t r[kWords];
+      load_words(g, r);
+      unpack(r, v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e) {
+        const int64_t j = j0 + e;
+        v[e] = (j >= 0 && j < V) ? at(j) : kNegInf;
+      }
+    }
+  }
+};
+
+template <>
+struct RowView<float> {
+  static constexpr int kBytes = 4;
+  const float* row;
+  const unsigned char* base;  // group 0, aligned to 64 bytes
+  int off;
+  int64_t V;
+  int NG;
+  __device__ __forceinline__ void init(const void* logits, int64_t src, int64_t stride, int64_t vocab) {
+    row = static_cast<const float*>(logits) + src * stride;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    base = reinterpret_cast<const unsigned char*>(a & ~uintptr_t(63));
+    off = (int)((a - reinterpret_cast<uintptr_t>(base)) / 4);
+    V = vocab;
+    NG = (int)((off + vocab + kGroup - 1) / kGroup);
+  }
+  __device__ __forceinline__ int64_t index(int g, int e) const { return (int64_t)g * kGroup - off + e; }
+  static constexpr int kWords = 16;
+  __device__ __forceinline__ float at(int64_t j) const { return row[j]; }
+  __device__ __forceinline__ bool full(int g) const {
+    const int64_t j0 = index(g, 0);
+    return j0 >= 0 && j0 + kGroup <= V;
+  }
+  __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords]) const {
+    ld256(base + (size_t)g * 64, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
+    ld256(base + (size_t)g * 64 + 32, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
+  }
+  __device__ __forceinline__ static void unpack(const uint32_t (&w)[kWords], float (&v)[kGroup]) {
+#pragma unroll
+    for (int q = 0; q < kGroup; ++q) v[q] = __uint_as_float(w[q]);
+  }
+  __device__ __forceinline__ void load(int g, float (&v)[kGroup]) const {
+    const int64_t j0 = index(g, 0);
+    if (j0 >= 0 && j0 + kGroup <= V) {
+      uint32_t r[kWords];
+      load_words(g, r);
+      unpack(r, v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e) {
+        const int64_t j = j0 + e;
+        v[e] = (j >= 0 && j < V) ? at(j) : kNegInf;
+      }
+    }
+  }
+};
+
+template <typename TIn>
+struct KeyOf {
+  using type = KeyOps<TIn>;
+};
+
+__device__ __forceinline__ float max16(const float (&v)[kGroup]) {
+  float a = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+  float b = fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7]));
+  float c = fmaxf(fmaxf(v[8], v[9]), fmaxf(v[10], v[11]));
+  float d = fmaxf(fmaxf(v[12], v[13]), fmaxf(v[14], v[15]));
+  return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
+// Visit every row entry whose value is >= lo (NaN never qualifies), looking
+// only at groups whose maximum is >= lo.  Candidate groups are re-read from
+// global memory (normally still in L2 after the streaming pass).
+template <typename TIn, typename F>
+__device__ __forceinline__ void visit_candidates(const RowView<TIn>& rv, const float* gmax, float lo, F&& f) {
+  for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
+    if (gmax[g] >= lo) {
+      float v[kGroup];
+      rv.load(g, v);
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e)
+        if (v[e] >= lo) f(v[e], rv.index(g, e));
+    }
+  }
+}
+
+// Find the highest bin b with above + sum_{b' >= b} hist[b'] >= target.  Writes
+// sh.cut_bin (-1 when the total never reaches target), sh.cut_above (weight
+// strictly above bin b, including `above`) and sh.cut_mass (hist[b]).
+__device__ __forceinline__ void find_cut_bin(Shared& sh, int nb, unsigned long long above, unsigned long long target) {
+  const int t = threadIdx.x;
+  const int top = nb - 1 - t * kBinsPerThread;
+  unsigned long long local = 0;
+#pragma unroll
+  for (int q = 0; q < kBinsPerThread; ++q) {
+    const int b = top - q;
+    if (b >= 0) local += sh.hist[b];
+  }
+  if (t == 0) sh.cut_bin = -1;
+  unsigned long long cum = above + block_exclusive_scan(local, sh.red_u64);
+  if (cum < target && cum + local >= target) {
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+      const int b = top - q;
+      if (b < 0) break;
+      const unsigned long long h = sh.hist[b];
+      if (cum + h >= target) {
+        sh.cut_bin = b;
+        sh.cut_above = cum;
+        sh.cut_mass = h;
+        break;
+      }
+      cum += h;
+    }
+  }
+  __syncthreads();
+}
+
+struct SelResult {
+  uint32_t key;                 // kept set: entries with key >= this
+  unsigned long long mass_ge;   // weight of the kept entries
+};
+
+// Exact threshold select over the row entries with keys in [klo, khi]:
+// returns the largest key kappa such that (weight of entries with key in
+// [kappa, khi]) >= target, where weight is 1 (top-k, target = k) or the
+// fixed-point probability mass exp((l - M)/T) * 2^40 (top-p).  With
+// joint_p >= 0 the target is joint_p * (total weight of the range), taken from
+// the first level's histogram.  Each level splits the remaining key range into
+// at most 2048 bins: bf16 keys (16 bits) need at most two levels, fp32 keys at
+// most three.  If the total weight never reaches the target (possible only
+// through rounding of a top-p target) the whole range is kept.
+template <typename TIn, bool kMass>
+__device__ SelResult radix_select(Shared& sh, const RowView<TIn>& rv, const float* gmax, uint32_t klo, uint32_t khi,
+                                  unsigned long long target, float joint_p, float M, float c) {
+  using K = KeyOps<TIn>;
+  unsigned long long above = 0, mass_at = 0;
+  bool first = true;
+  do {
+    const uint32_t width = khi - klo;
+    const int bits = width ? 32 - __clz(width) : 0;
+    const int shift = bits > kBinBits ? bits - kBinBits : 0;
+    const int nb = (int)(width >> shift) + 1;
+    for (int b = threadIdx.x; b < nb; b += kThreads) sh.hist[b] = 0ull;
+    __syncthreads();
+    const float lo = K::value(klo), hi = K::value(khi);
+    const uint32_t base = klo, top = khi;
+    visit_candidates(rv, gmax, lo, [&](float v, int64_t) {
+      const uint32_t kk = K::key(v);
+      if (v <= hi && kk >= base && kk <= top) {
+        unsigned long long w = 1ull;
+        if (kMass) w = __float2ull_rn(exp2f((v - M) * c) * kMassScale);
+        atomicAdd(&sh.hist[(kk - base) >> shift], w);
+      }
+    });
+    __syncthreads();
+    if (first && joint_p >= 0.f) {
+      unsigned long long part = 0;
+      for (int b = threadIdx.x; b < nb; b += kThreads) part += sh.hist[b];
+      const unsigned long long total = block_reduce(part, OpAddU64(), sh.red_u64);
+      target = __float2ull_ru(joint_p * __ull2float_rn(total));
+    }
+    if (target < 1ull) target = 1ull;
+    find_cut_bin(sh, nb, above, target);
+    const int b = sh.cut_bin;
+    if (b < 0) {  // only reachable on the first level
+      unsigned long long part = 0;
+      for (int q = threadIdx.x; q < nb; q += kThreads) part += sh.hist[q];
+      const unsigned long long total = block_reduce(part, OpAddU64(), sh.red_u64);
+      return SelResult{klo, total};
+    }
+    above = sh.cut_above;
+    mass_at = sh.cut_mass;
+    const uint32_t nlo = klo + ((uint32_t)b << shift);
+    const unsigned long long nhi = (unsigned long long)nlo + ((1ull << shift) - 1ull);
+    khi = nhi < (unsigned long long)khi ? (uint32_t)nhi : khi;
+    klo = nlo;
+    first = false;
+    __syncthreads();
+  } while (klo < khi);
+  return SelResult{klo, above + mass_at};
+}
+
+// A value gamma such that at least k of the threads' running maxima are
+// >= gamma (hence at least k row entries are), within one histogram bin of the
+// k-th largest thread maximum; -inf when fewer than k threads saw a finite
+// entry.  It bounds the top-k cut from below.
+template <typename TIn>
+__device__ float thread_max_bound(Shared& sh, float m, int k) {
+  using K = KeyOps<TIn>;
+  const bool fin = m > kNegInf;
+  const int F = block_reduce(fin ? 1 : 0, OpAddI(), sh.red_i);
+  if (F < k) return kNegInf;
+  const float mn = block_reduce(fin ? m : kPosInf, OpMin(), sh.red_f);
+  const float mx = block_reduce(m, OpMax(), sh.red_f);
+  const uint32_t klo = K::key(mn), khi = K::key(mx);
+  const uint32_t width = khi - klo;
+  const int bits = width ? 32 - __clz(width) : 0;
+  const int shift = bits > kBinBits ? bits - kBinBits : 0;
+  const int nb = (int)(width >> shift) + 1;
+  for (int b = threadIdx.x; b < nb; b += kThreads) sh.hist[b] = 0ull;
+  __syncthreads();
+  if (fin) atomicAdd(&sh.hist[(K::key(m) - klo) >> shift], 1ull);
+  __syncthreads();
+  find_cut_bin(sh, nb, 0ull, (unsigned long long)k);
+  const int b = sh.cut_bin;
+  __syncthreads();
+  return b < 0 ? kNegInf : K::value(klo + ((uint32_t)b << shift));
+}
+
+__device__ __forceinline__ void row_error(const KernelArgs& a, int64_t i, int mode, int err) {
+  if (threadIdx.x == 0) {
+    if (mode == MODE_SAMPLE) a.out_ids[i] = -1;
+    if (a.error_word) atomicOr(a.error_word, err);
+  }
+  if (mode == MODE_LOGPROBS) {
+    float* out = a.out_lp + i * a.vocab;
+    const float nan = __uint_as_float(0x7FC00000u);
+    for (int64_t j = threadIdx.x; j < a.vocab; j += kThreads) out[j] = nan;
+  }
+}
+
+// Write out[j] = kept(v_j) ? value(v_j) : -inf over the whole row, with
+// 16-byte stores to the output where its alignment allows.
+template <typename TIn, typename KeptF, typename ValF>
+__device__ __forceinline__ void write_row(const RowView<TIn>& rv, float* out, KeptF kept, ValF val) {
+  const int64_t V = rv.V;
+  const uintptr_t oa = reinterpret_cast<uintptr_t>(out);
+  int64_t head = (int64_t)(((16u - (oa & 15u)) & 15u) / 4u);
+  if ((oa & 3u) != 0u) head = V;  // not even float aligned: all scalar
+  if (head > V) head = V;
+  for (int64_t j = threadIdx.x; j < head; j += kThreads) {
+    const float v = rv.at(j);
+    out[j] = kept(v) ? val(v) : kNegInf;
+  }
+  const int64_t nq = (V - head) / 4;
+  for (int64_t q = threadIdx.x; q < nq; q += kThreads) {
+    const int64_t j = head + 4 * q;
+    float4 o;
+    float v0 = rv.at(j), v1 = rv.at(j + 1), v2 = rv.at(j + 2), v3 = rv.at(j + 3);
+    o.x = kept(v0) ? val(v0) : kNegInf;
+    o.y = kept(v1) ? val(v1) : kNegInf;
+    o.z = kept(v2) ? val(v2) : kNegInf;
+    o.w = kept(v3) ? val(v3) : kNegInf;
+    *reinterpret_cast<float4*>(out + j) = o;
+  }
+  for (int64_t j = head + 4 * nq + threadIdx.x; j < V; j += kThreads) {
+    const float v = rv.at(j);
+    out[j] = kept(v) ? val(v) : kNegInf;
+  }
+}
+
+template <typename TIn, int ROUTE, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelArgs a) {
+  using K = KeyOps<TIn>;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  float* gmax = reinterpret_cast<float*>(smem_raw + sizeof(Shared));
+  const int tid = threadIdx.x;
+  const int64_t i = blockIdx.x;
+
+  // ---- row -> (logits row, request) ------------------------------------
+  int err = 0;
+  int64_t src = i;
+  if (a.gather) {
+    src = a.gather[i];
+    if (src < 0 || src >= a.logits_rows) err |= LS_ROW_ERR_BAD_GATHER;
+  }
+  int64_t req = i;
+  if (a.map_mode == MAP_T2R) {
+    req = a.t2r[i];
+  } else if (a.map_mode == MAP_SPEC) {
+    req = i < a.spec_decode_rows ? i / a.spec_per_req : a.spec_num_decode + (i - a.spec_decode_rows);
+  }
+  if (a.out_t2r && tid == 0) a.out_t2r[i] = (int32_t)req;
+  if (req < 0 || req >= a.num_requests) err |= LS_ROW_ERR_BAD_REQUEST;
+  if (err) {
+    row_error(a, i, MODE, err);
+    return;
+  }
+
+  const float T = a.temperature[req];
+  const int32_t k = a.top_k[req];
+  const float p = a.top_p[req];
+  const int64_t V = a.vocab;
+  const bool greedy = !(T >= 1e-5f);
+  const bool k_on = !greedy && (ROUTE & ROUTE_K) && k >= 1 && (int64_t)k < V;
+  const bool p_on = !greedy && (ROUTE & ROUTE_P) && p < 0.99999f;
+  const bool need_sum = !greedy && !k_on && (p_on || MODE == MODE_LOGPROBS);
+  const float c = greedy ? 0.f : kLog2e / T;
+
+  RowView<TIn> rv;
+  rv.init(a.logits, src, a.stride, V);
+
+  // ---- streaming pass: group maxima, running max, online mass ----------
+  float m = kNegInf, s = 0.f;
+  constexpr int U = RowView<TIn>::kBytes == 2 ? 4 : 2;
+  for (int g0 = tid; g0 < rv.NG; g0 += kThreads * U) {
+    uint32_t w[U][RowView<TIn>::kWords];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + u * kThreads;
+      if (g < rv.NG && rv.full(g)) rv.load_words(g, w[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + u * kThreads;
+      if (g < rv.NG) {
+        float v[kGroup];
+        if (rv.full(g)) {
+          RowView<TIn>::unpack(w[u], v);
+        } else {
+          rv.load(g, v);
+        }
+        const float gm = max16(v);
+        gmax[g] = gm;
+        if (need_sum) {
+          if (gm > m) {
+            s *= exp2f((m - gm) * c);
+            m = gm;
+          }
+          if (gm > kNegInf) {
+            // four interleaved partial sums of four terms each, then a tree
+            float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+#pragma unroll
+            for (int q = 0; q < kGroup; q += 4) {
+              e0 += exp2f((v[q] - m) * c);
+              e1 += exp2f((v[q + 1] - m) * c);
+              e2 += exp2f((v[q + 2] - m) * c);
+              e3 += exp2f((v[q + 3] - m) * c);
+            }
+            s += (e0 + e1) + (e2 + e3);
+          }
+        } else {
+          m = fmaxf(m, gm);
+        }
+      }
+    }
+  }
+  const float M = block_reduce(m, OpMax(), sh.red_f);  // NaN entries are ignored by fmaxf
+  if (M == kNegInf) {
+    row_error(a, i, MODE, LS_ROW_ERR_NO_FINITE);
+    return;
+  }
+  if (tid == 0) {
+    sh.best = 0ull;
+    sh.acc = 0ull;
+    sh.min_index = 0x7FFFFFFF;
+  }
+  __syncthreads();
+
+  // ---- rows without a temperature-scaled distribution -------------------
+  // Greedy: the maximum's ties, lowest index.  +inf maximum: uniform over the
+  // +inf entries (the limit of the softmax), i.e. Gumbel-max with z = 0 there.
+  if (greedy || M == kPosInf) {
+    const bool use_noise = !greedy;
+    const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;
+    visit_candidates(rv, gmax, M, [&](float, int64_t j) {
+      if (MODE == MODE_LOGPROBS) {
+        atomicAdd(&sh.acc, 1ull);
+      } else if (use_noise) {
+        const float sc = gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j));
+        atomicMax(&sh.best, argmax_key(sc, j));
+      } else {
+        atomicMin(&sh.min_index, (int)j);
+      }
+    });
+    __syncthreads();
+    if (MODE == MODE_SAMPLE) {
+      if (tid == 0) a.out_ids[i] = use_noise ? argmax_index(sh.best) : sh.min_index;
+    } else {
+      const float lp = -logf((float)sh.acc);
+      write_row(rv, a.out_lp + i * V, [&](float v) { return v >= M; }, [&](float) { return lp; });
+    }
+    return;
+  }
+
+  // ---- total mass (top-p without top-k, and unfiltered log-probs) -------
+  float S = 0.f;
+  if (need_sum) {
+    const float st = m > kNegInf ? s * exp2f((m - M) * c) : 0.f;
+    S = block_reduce(st, OpAddF(), sh.red_f);
+    if (!(S <= FLT_MAX)) {
+      // A NaN entry poisoned the online sum: recompute it reading NaN as -inf.
+      float acc = 0.f;
+      for (int g = tid; g < rv.NG; g += kThreads) {
+        float v[kGroup];
+        rv.load(g, v);
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) {
+          const float x = v[q] == v[q] ? v[q] : kNegInf;
+          acc += exp2f((x - M) * c);
+        }
+      }
+      S = block_reduce(acc, OpAddF(), sh.red_f);
+    }
+  }
+
+  // ---- exact top-k and top-p cuts ---------------------------------------
+  const uint32_t key_max = K::key(M);
+  uint32_t lo_key = K::key(-FLT_MAX);  // no filter: every finite entry
+  unsigned long long kept_mass = 0ull;
+  if (k_on) {
+    const float gamma = thread_max_bound<TIn>(sh, m, k);
+    const uint32_t klo = gamma > kNegInf ? K::key(gamma) : K::key(-FLT_MAX);
+    lo_key = radix_select<TIn, false>(sh, rv, gmax, klo, key_max, (unsigned long long)k, -1.f, M, c).key;
+  }
+  if (p_on) {
+    SelResult r;
+    if (k_on) {
+      r = radix_select<TIn, true>(sh, rv, gmax, lo_key, key_max, 0ull, fmaxf(p, 0.f), M, c);
+    } else {
+      // Every entry below Lp carries less than (1 - p) S e^-2 in total, so the
+      // cut lies at or above it.
+      float Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
+      Lp = fminf(fmaxf(Lp, -FLT_MAX), M);
+      const unsigned long long target = __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale);
+      r = radix_select<TIn, true>(sh, rv, gmax, K::key(Lp), key_max, target, -1.f, M, c);
+    }
+    lo_key = r.key;
+    kept_mass = r.mass_ge;
+  }
+  const float lo_val = K::value(lo_key);
+
+  if (MODE == MODE_SAMPLE) {
+    // ---- Gumbel-max over the kept set ------------------------------------
+    const uint64_t seed = a.seed[req];
+    const float lg = fmaxf(lo_val, M - kGumbelSpan * T);
+    visit_candidates(rv, gmax, lg, [&](float v, int64_t j) {
+      const float sc = __fdiv_rn(v, T) + gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j));
+      atomicMax(&sh.best, argmax_key(sc, j));
+    });
+    __syncthreads();
+    if (tid == 0) a.out_ids[i] = argmax_index(sh.best);
+  } else {
+    // ---- log-probs of the processed distribution -------------------------
+    float lnS;
+    if (p_on) {
+      lnS = logf(__ull2float_rn(kept_mass) / kMassScale);
+    } else if (k_on) {
+      visit_candidates(rv, gmax, lo_val, [&](float v, int64_t) {
+        atomicAdd(&sh.acc, __float2ull_rn(exp2f((v - M) * c) * kMassScale));
+      });
+      __syncthreads();
+      lnS = logf(__ull2float_rn(sh.acc) / kMassScale);
+    } else {
+      lnS = logf(S);
+    }
+    write_row(rv, a.out_lp + i * V, [&](float v) { return v >= lo_val; },
+              [&](float v) { return __fdiv_rn(v - M, T) - lnS; });
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static size_t smem_bytes(int64_t vocab, int elem_bytes) {
+  // worst-case group count over row alignments
+  const int64_t off_max = (elem_bytes == 2 ? 32 : 64) / elem_bytes - 1;
+  const int64_t ng = (off_max + vocab + kGroup - 1) / kGroup;
+  return sizeof(Shared) + (size_t)ng * sizeof(float);
+}
+
+static int max_dyn_smem() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  return v;
+}
+
+template <typename TIn, int ROUTE, int MODE>
+static ls_status launch_rows(const KernelArgs& a, int32_t n, size_t smem, cudaStream_t stream) {
+  auto kern = sampler_row_kernel<TIn, ROUTE, MODE>;
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return LS_ERR_CUDA;
+  }
+  kern<<<dim3((unsigned)n), dim3(kThreads), smem, stream>>>(a);
+  return cudaPeekAtLastError() == cudaSuccess ? LS_OK : LS_ERR_CUDA;
+}
+
+template <int MODE>
+static ls_status dispatch(const KernelArgs& a, ls_dtype dtype, int route, int32_t n, cudaStream_t stream) {
+  const size_t smem = smem_bytes(a.vocab, dtype == LS_DTYPE_BF16 ? 2 : 4);
+  const int lim = max_dyn_smem();
+  if (lim <= 0) return LS_ERR_CUDA;
+  if (smem > (size_t)lim) return LS_ERR_UNSUPPORTED;
+  if (dtype == LS_DTYPE_BF16) {
+    switch (route) {
+      case ROUTE_NONE: return launch_rows<bf16_tag, ROUTE_NONE, MODE>(a, n, smem, stream);
+      case ROUTE_K: return launch_rows<bf16_tag, ROUTE_K, MODE>(a, n, smem, stream);
+      case ROUTE_P: return launch_rows<bf16_tag, ROUTE_P, MODE>(a, n, smem, stream);
+      default: return launch_rows<bf16_tag, ROUTE_KP, MODE>(a, n, smem, stream);
+    }
+  }
+  switch (route) {
+    case ROUTE_NONE: return launch_rows<float, ROUTE_NONE, MODE>(a, n, smem, stream);
+    case ROUTE_K: return launch_rows<float, ROUTE_K, MODE>(a, n, smem, stream);
+    case ROUTE_P: return launch_rows<float, ROUTE_P, MODE>(a, n, smem, stream);
+    default: return launch_rows<float, ROUTE_KP, MODE>(a, n, smem, stream);
+  }
+}
+
+static bool params_ok(const ls_params* prm, bool need_seed) {
+  return prm && prm->temperature && prm->top_k && prm->top_p && (!need_seed || prm->seed) && prm->num_requests >= 1;
+}
+
+static bool common_ok(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride) {
+  return logits && (dtype == LS_DTYPE_F32 || dtype == LS_DTYPE_BF16) && vocab >= 1 && row_stride >= vocab &&
+         logits_rows >= 1 && vocab <= 0x7FFFFFF0ll;
+}
+
+static KernelArgs make_args(const void* logits, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                            const int32_t* gather, const ls_params* prm, uint64_t step, int32_t* error_word) {
+  KernelArgs a{};
+  a.logits = logits;
+  a.logits_rows = logits_rows;
+  a.vocab = vocab;
+  a.stride = row_stride;
+  a.gather = gather;
+  a.temperature = prm->temperature;
+  a.top_k = prm->top_k;
+  a.top_p = prm->top_p;
+  a.seed = prm->seed;
+  a.num_requests = prm->num_requests;
+  a.step = step;
+  a.error_word = error_word;
+  return a;
+}
+
+}  // namespace lsg
+
+using namespace lsg;
+
+extern "C" {
+
+ls_status ls_sample(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                    int32_t n, const int32_t* gather_indices, const int32_t* token_to_request_index,
+                    const ls_params* params, uint64_t step, int no_top_k, int no_top_p, int32_t* out_ids,
+                    int32_t* error_word, void* stream) {
+  if (n < 0) return LS_ERR_INVALID_ARG;
+  if (n == 0) return LS_OK;
+  if (!common_ok(logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, true) || !out_ids)
+    return LS_ERR_INVALID_ARG;
+  if (!gather_indices && (int64_t)n > logits_rows) return LS_ERR_INVALID_ARG;
+  if (!token_to_request_index && n > params->num_requests) return LS_ERR_INVALID_ARG;
+  KernelArgs a = make_args(logits, logits_rows, vocab, row_stride, gather_indices, params, step, error_word);
+  a.t2r = token_to_request_index;
+  a.map_mode = token_to_request_index ? MAP_T2R : MAP_IDENTITY;
+  a.out_ids = out_ids;
+  const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
+  return dispatch<MODE_SAMPLE>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
+}
+
+ls_status ls_sample_speculative(const void* required_logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
+                                int64_t row_stride, int32_t num_decode, int32_t num_prefill,
+                                int32_t num_speculative_tokens, const int32_t* gather_indices,
+                                const ls_params* params, uint64_t step, int no_top_k, int no_top_p,
+                                int32_t* out_ids, int32_t* out_token_to_request_index, int32_t* error_word,
+                                void* stream) {
+  if (num_decode < 0 || num_prefill < 0 || num_speculative_tokens < 0) return LS_ERR_INVALID_ARG;
+  const int64_t per = 1 + (int64_t)num_speculative_tokens;
+  const int64_t n64 = (int64_t)num_decode * per + num_prefill;
+  if (n64 > 0x7FFFFFFFll) return LS_ERR_INVALID_ARG;
+  const int32_t n = (int32_t)n64;
+  if (n == 0) return LS_OK;
+  if (!common_ok(required_logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, true) || !out_ids)
+    return LS_ERR_INVALID_ARG;
+  if (!gather_indices && n64 > logits_rows) return LS_ERR_INVALID_ARG;
+  if ((int64_t)num_decode + num_prefill > params->num_requests) return LS_ERR_INVALID_ARG;
+  KernelArgs a = make_args(required_logits, logits_rows, vocab, row_stride, gather_indices, params, step,
+                           error_word);
+  a.map_mode = MAP_SPEC;
+  a.spec_decode_rows = (int32_t)((int64_t)num_decode * per);
+  a.spec_per_req = (int32_t)per;
+  a.spec_num_decode = num_decode;
+  a.out_ids = out_ids;
+  a.out_t2r = out_token_to_request_index;
+  const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
+  return dispatch<MODE_SAMPLE>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
+}
+
+ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                       int32_t num_rows, const int32_t* gather_indices, const int32_t* token_to_request_index,
+                       const ls_params* params, float* out_log_probs, int32_t* error_word, void* stream) {
+  if (num_rows < 0) return LS_ERR_INVALID_ARG;
+  if (num_rows == 0) return LS_OK;
+  if (!common_ok(logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, false) || !out_log_probs)
+    return LS_ERR_INVALID_ARG;
+  if (!gather_indices && (int64_t)num_rows > logits_rows) return LS_ERR_INVALID_ARG;
+  if (!token_to_request_index && num_rows > params->num_requests) return LS_ERR_INVALID_ARG;
+  KernelArgs a = make_args(logits, logits_rows, vocab, row_stride, gather_indices, params, 0, error_word);
+  a.t2r = token_to_request_index;
+  a.map_mode = token_to_request_index ? MAP_T2R : MAP_IDENTITY;
+  a.out_lp = out_log_probs;
+  return dispatch<MODE_LOGPROBS>(a, dtype, ROUTE_KP, num_rows, static_cast<cudaStream_t>(stream));
+}
+
+const char* ls_status_string(ls_status s) {
+  switch (s) {
+    case LS_OK: return "LS_OK";
+    case LS_ERR_INVALID_ARG: return "LS_ERR_INVALID_ARG: invalid argument (nothing launched)";
+    case LS_ERR_UNSUPPORTED: return "LS_ERR_UNSUPPORTED: vocab beyond the shared-memory limit of this device";
+    case LS_ERR_CUDA: return "LS_ERR_CUDA: CUDA launch failed";
+    default: return "unknown ls_status";
+  }
+}
+
+int64_t ls_max_vocab(ls_dtype dtype) {
+  const int lim = max_dyn_smem();
+  if (lim <= 0) return 0;
+  const int eb = dtype == LS_DTYPE_BF16 ? 2 : 4;
+  const int64_t off_max = (eb == 2 ? 32 : 64) / eb - 1;
+  const int64_t ng = ((int64_t)lim - (int64_t)sizeof(Shared)) / (int64_t)sizeof(float);
+  return ng * kGroup - off_max - (kGroup - 1);
+}
+
+}  // extern "C"

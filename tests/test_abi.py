@@ -1,0 +1,97 @@
+"""The C ABI library on a host without a GPU: it builds, loads, exports every
+entry point include/*.h declares, and rejects bad arguments on the host before
+any CUDA call."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from logits_sampling_gb300 import build as b
+    path = b.build()
+    from logits_sampling_gb300 import _binding
+    return _binding.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z_0-9]*\s*\*?\s+(ls_[a-z_0-9]+)\s*\(", text, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_three_calls():
+    names = _declared_functions()
+    assert {"ls_sample", "ls_sample_speculative", "ls_log_probs", "ls_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_no_torch_in_the_abi():
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        assert "at::" not in text and "torch::" not in text and "Tensor" not in text
+
+
+def test_host_validation_before_any_launch(lib):
+    from logits_sampling_gb300._binding import _Params
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: every call below fails validation first
+    prm = _Params(fake, fake, fake, fake, 4)
+    byref = ctypes.byref
+    # n < 0
+    assert lib.ls_sample(fake, 0, 4, 10, 10, -1, None, None, byref(prm), 0, 0, 0, fake, None, None) == 1
+    # n == 0: OK, nothing launched
+    assert lib.ls_sample(fake, 0, 4, 10, 10, 0, None, None, byref(prm), 0, 0, 0, fake, None, None) == 0
+    # null logits, bad dtype, vocab < 1, stride < vocab, null out
+    assert lib.ls_sample(None, 0, 4, 10, 10, 2, None, None, byref(prm), 0, 0, 0, fake, None, None) == 1
+    assert lib.ls_sample(fake, 7, 4, 10, 10, 2, None, None, byref(prm), 0, 0, 0, fake, None, None) == 1
+    assert lib.ls_sample(fake, 0, 4, 0, 10, 2, None, None, byref(prm), 0, 0, 0, fake, None, None) == 1
+    assert lib.ls_sample(fake, 0, 4, 10, 9, 2, None, None, byref(prm), 0, 0, 0, fake, None, None) == 1
+    assert lib.ls_sample(fake, 0, 4, 10, 10, 2, None, None, byref(prm), 0, 0, 0, None, None, None) == 1
+    # n > logits_rows without gather; n > num_requests without a mapping
+    assert lib.ls_sample(fake, 0, 4, 10, 10, 5, None, None, byref(prm), 0, 0, 0, fake, None, None) == 1
+    prm2 = _Params(fake, fake, fake, fake, 2)
+    assert lib.ls_sample(fake, 0, 4, 10, 10, 3, None, None, byref(prm2), 0, 0, 0, fake, None, None) == 1
+    # missing parameter arrays
+    prm3 = _Params(fake, None, fake, fake, 4)
+    assert lib.ls_sample(fake, 0, 4, 10, 10, 2, None, None, byref(prm3), 0, 0, 0, fake, None, None) == 1
+    # speculative: negative counts, too many rows / requests
+    assert lib.ls_sample_speculative(fake, 1, 4, 10, 10, -1, 0, 0, None, byref(prm), 0, 0, 0, fake, None, None,
+                                     None) == 1
+    assert lib.ls_sample_speculative(fake, 1, 4, 10, 10, 2, 1, 1, None, byref(prm), 0, 0, 0, fake, None, None,
+                                     None) == 1
+    assert lib.ls_sample_speculative(fake, 1, 100, 10, 10, 3, 2, 0, None, byref(prm), 0, 0, 0, fake, None, None,
+                                     None) == 1
+    assert lib.ls_sample_speculative(fake, 1, 100, 10, 10, 0, 0, 3, None, byref(prm), 0, 0, 0, fake, None, None,
+                                     None) == 0
+    # log-probs
+    assert lib.ls_log_probs(fake, 1, 4, 10, 10, -2, None, None, byref(prm), fake, None, None) == 1
+    assert lib.ls_log_probs(fake, 1, 4, 10, 10, 0, None, None, byref(prm), fake, None, None) == 0
+    assert lib.ls_log_probs(fake, 1, 4, 10, 10, 2, None, None, byref(prm), None, None, None) == 1
+
+
+def test_status_strings(lib):
+    for s in range(4):
+        assert lib.ls_status_string(s)
+    assert b"INVALID" in lib.ls_status_string(1)
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from logits_sampling_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "PKG", str(tmp_path))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _binding.load_library()
