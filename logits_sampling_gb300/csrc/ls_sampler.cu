@@ -54,6 +54,7 @@ struct KernelArgs {
   int32_t* out_t2r;
   float* out_lp;
   int32_t* error_word;
+  int32_t cand_cap;  // capacity of the shared-memory candidate list
 };
 
 // Fixed part of the dynamic shared memory; the group maxima follow it.
@@ -68,6 +69,7 @@ struct Shared {
   unsigned long long cut_mass;
   int cut_bin;
   int min_index;
+  int cand_count;
 };
 
 // ---------------------------------------------------------------------------
@@ -210,6 +212,63 @@ __device__ __forceinline__ void visit_candidates(const RowView<TIn>& rv, const f
   }
 }
 
+// The row entries that later phases examine.  After the streaming pass one
+// visit of the candidate groups copies every entry >= the row's candidate
+// bound into a shared-memory list (value, index); all later phases then read
+// that list.  If the list would overflow, phases fall back to re-reading the
+// candidate groups from global memory.
+template <typename TIn>
+struct Cands {
+  const RowView<TIn>* rv;
+  const float* gmax;
+  const float* lv;
+  const int32_t* lj;
+  int count;
+  bool listed;
+  template <typename F>
+  __device__ __forceinline__ void each(float lo, F&& f) const {
+    if (listed) {
+      for (int c = threadIdx.x; c < count; c += kThreads) {
+        const float v = lv[c];
+        if (v >= lo) f(v, (int64_t)lj[c]);
+      }
+    } else {
+      visit_candidates(*rv, gmax, lo, f);
+    }
+  }
+};
+
+// Copy the entries >= lo into the list; returns the candidate source.
+template <typename TIn>
+__device__ Cands<TIn> collect_candidates(Shared& sh, const RowView<TIn>& rv, const float* gmax, float lo, float* lv,
+                                         int32_t* lj, int cap) {
+  if (threadIdx.x == 0) sh.cand_count = 0;
+  __syncthreads();
+  for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
+    if (gmax[g] >= lo) {
+      float v[kGroup];
+      rv.load(g, v);
+      int cnt = 0;
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e) cnt += v[e] >= lo ? 1 : 0;
+      int slot = atomicAdd(&sh.cand_count, cnt);
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e) {
+        if (v[e] >= lo) {
+          if (slot < cap) {
+            lv[slot] = v[e];
+            lj[slot] = (int32_t)rv.index(g, e);
+          }
+          ++slot;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int count = sh.cand_count;
+  return Cands<TIn>{&rv, gmax, lv, lj, count, count <= cap};
+}
+
 // Find the highest bin b with above + sum_{b' >= b} hist[b'] >= target.  Writes
 // sh.cut_bin (-1 when the total never reaches target), sh.cut_above (weight
 // strictly above bin b, including `above`) and sh.cut_mass (hist[b]).
@@ -257,7 +316,7 @@ struct SelResult {
 // most three.  If the total weight never reaches the target (possible only
 // through rounding of a top-p target) the whole range is kept.
 template <typename TIn, bool kMass>
-__device__ SelResult radix_select(Shared& sh, const RowView<TIn>& rv, const float* gmax, uint32_t klo, uint32_t khi,
+__device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo, uint32_t khi,
                                   unsigned long long target, float joint_p, float M, float c) {
   using K = KeyOps<TIn>;
   unsigned long long above = 0, mass_at = 0;
@@ -271,7 +330,7 @@ __device__ SelResult radix_select(Shared& sh, const RowView<TIn>& rv, const floa
     __syncthreads();
     const float lo = K::value(klo), hi = K::value(khi);
     const uint32_t base = klo, top = khi;
-    visit_candidates(rv, gmax, lo, [&](float v, int64_t) {
+    cs.each(lo, [&](float v, int64_t) {
       const uint32_t kk = K::key(v);
       if (v <= hi && kk >= base && kk <= top) {
         unsigned long long w = 1ull;
@@ -383,6 +442,9 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   float* gmax = reinterpret_cast<float*>(smem_raw + sizeof(Shared));
   const int tid = threadIdx.x;
+  const int64_t ng_cap = (a.vocab + 2 * kGroup - 1) / kGroup;  // group maxima: worst-case row alignment
+  float* cand_v = gmax + ng_cap;
+  int32_t* cand_j = reinterpret_cast<int32_t*>(cand_v + a.cand_cap);
   const int64_t i = blockIdx.x;
 
   // ---- row -> (logits row, request) ------------------------------------
@@ -481,7 +543,8 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   if (greedy || M == kPosInf) {
     const bool use_noise = !greedy;
     const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;
-    visit_candidates(rv, gmax, M, [&](float, int64_t j) {
+    const Cands<TIn> cs = collect_candidates(sh, rv, gmax, M, cand_v, cand_j, a.cand_cap);
+    cs.each(M, [&](float, int64_t j) {
       if (MODE == MODE_LOGPROBS) {
         atomicAdd(&sh.acc, 1ull);
       } else if (use_noise) {
@@ -522,26 +585,43 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     }
   }
 
-  // ---- exact top-k and top-p cuts ---------------------------------------
+  // ---- candidate bound, candidate list ---------------------------------
+  // Every entry that any later phase needs is >= lc:
+  //  * top-k: at least k thread maxima (hence k entries) are >= gamma;
+  //  * top-p alone: the entries below Lp carry less than (1 - p) S e^-2, so
+  //    the cut lies above Lp;
+  //  * no filter: an entry with z more than the noise span below max z can
+  //    never beat the maximum's perturbed score.
   const uint32_t key_max = K::key(M);
+  const float lg = M - kGumbelSpan * T;
+  float lc = lg;
+  float gamma = kNegInf;
+  if (k_on) {
+    gamma = thread_max_bound<TIn>(sh, m, k);
+    lc = gamma > kNegInf ? gamma : -FLT_MAX;
+  } else if (p_on) {
+    float Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
+    lc = fminf(fmaxf(Lp, -FLT_MAX), M);
+  } else if (MODE == MODE_LOGPROBS) {
+    lc = kPosInf;  // unfiltered log-probs need no candidates
+  }
+  lc = fmaxf(lc, -FLT_MAX);
+  const Cands<TIn> cs = (lc <= M) ? collect_candidates(sh, rv, gmax, lc, cand_v, cand_j, a.cand_cap)
+                                  : Cands<TIn>{&rv, gmax, cand_v, cand_j, 0, true};
+
+  // ---- exact top-k and top-p cuts ---------------------------------------
   uint32_t lo_key = K::key(-FLT_MAX);  // no filter: every finite entry
   unsigned long long kept_mass = 0ull;
   if (k_on) {
-    const float gamma = thread_max_bound<TIn>(sh, m, k);
-    const uint32_t klo = gamma > kNegInf ? K::key(gamma) : K::key(-FLT_MAX);
-    lo_key = radix_select<TIn, false>(sh, rv, gmax, klo, key_max, (unsigned long long)k, -1.f, M, c).key;
+    lo_key = radix_select<TIn, false>(sh, cs, K::key(lc), key_max, (unsigned long long)k, -1.f, M, c).key;
   }
   if (p_on) {
     SelResult r;
     if (k_on) {
-      r = radix_select<TIn, true>(sh, rv, gmax, lo_key, key_max, 0ull, fmaxf(p, 0.f), M, c);
+      r = radix_select<TIn, true>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), M, c);
     } else {
-      // Every entry below Lp carries less than (1 - p) S e^-2 in total, so the
-      // cut lies at or above it.
-      float Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
-      Lp = fminf(fmaxf(Lp, -FLT_MAX), M);
       const unsigned long long target = __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale);
-      r = radix_select<TIn, true>(sh, rv, gmax, K::key(Lp), key_max, target, -1.f, M, c);
+      r = radix_select<TIn, true>(sh, cs, K::key(lc), key_max, target, -1.f, M, c);
     }
     lo_key = r.key;
     kept_mass = r.mass_ge;
@@ -551,8 +631,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   if (MODE == MODE_SAMPLE) {
     // ---- Gumbel-max over the kept set ------------------------------------
     const uint64_t seed = a.seed[req];
-    const float lg = fmaxf(lo_val, M - kGumbelSpan * T);
-    visit_candidates(rv, gmax, lg, [&](float v, int64_t j) {
+    cs.each(fmaxf(lo_val, lg), [&](float v, int64_t j) {
       const float sc = __fdiv_rn(v, T) + gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j));
       atomicMax(&sh.best, argmax_key(sc, j));
     });
@@ -564,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     if (p_on) {
       lnS = logf(__ull2float_rn(kept_mass) / kMassScale);
     } else if (k_on) {
-      visit_candidates(rv, gmax, lo_val, [&](float v, int64_t) {
+      cs.each(lo_val, [&](float v, int64_t) {
         atomicAdd(&sh.acc, __float2ull_rn(exp2f((v - M) * c) * kMassScale));
       });
       __syncthreads();
@@ -580,11 +659,21 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-static size_t smem_bytes(int64_t vocab, int elem_bytes) {
-  // worst-case group count over row alignments
-  const int64_t off_max = (elem_bytes == 2 ? 32 : 64) / elem_bytes - 1;
-  const int64_t ng = (off_max + vocab + kGroup - 1) / kGroup;
-  return sizeof(Shared) + (size_t)ng * sizeof(float);
+// Shared memory of one CTA: fixed part, group maxima (worst-case row
+// alignment), candidate list of `cap` (value, index) pairs.
+static size_t smem_bytes(int64_t vocab, int cap) {
+  const int64_t ng = (vocab + 2 * kGroup - 1) / kGroup;
+  return sizeof(Shared) + (size_t)ng * sizeof(float) + (size_t)cap * (sizeof(float) + sizeof(int32_t));
+}
+
+// Candidate-list capacity: up to 4096 entries while two CTAs still fit on an
+// SM, never below 256.
+static int cand_capacity(int64_t vocab) {
+  constexpr size_t kTwoPerSm = 112 * 1024;
+  const size_t base = smem_bytes(vocab, 0);
+  int cap = 4096;
+  while (cap > 256 && base + (size_t)cap * 8 > kTwoPerSm) cap -= 256;
+  return cap;
 }
 
 static int max_dyn_smem() {
@@ -606,8 +695,9 @@ static ls_status launch_rows(const KernelArgs& a, int32_t n, size_t smem, cudaSt
 }
 
 template <int MODE>
-static ls_status dispatch(const KernelArgs& a, ls_dtype dtype, int route, int32_t n, cudaStream_t stream) {
-  const size_t smem = smem_bytes(a.vocab, dtype == LS_DTYPE_BF16 ? 2 : 4);
+static ls_status dispatch(KernelArgs a, ls_dtype dtype, int route, int32_t n, cudaStream_t stream) {
+  a.cand_cap = cand_capacity(a.vocab);
+  const size_t smem = smem_bytes(a.vocab, a.cand_cap);
   const int lim = max_dyn_smem();
   if (lim <= 0) return LS_ERR_CUDA;
   if (smem > (size_t)lim) return LS_ERR_UNSUPPORTED;
@@ -733,12 +823,11 @@ const char* ls_status_string(ls_status s) {
 }
 
 int64_t ls_max_vocab(ls_dtype dtype) {
+  (void)dtype;  // the limit is the same for both dtypes: 4 bytes of shared memory per 16 logits
   const int lim = max_dyn_smem();
   if (lim <= 0) return 0;
-  const int eb = dtype == LS_DTYPE_BF16 ? 2 : 4;
-  const int64_t off_max = (eb == 2 ? 32 : 64) / eb - 1;
-  const int64_t ng = ((int64_t)lim - (int64_t)sizeof(Shared)) / (int64_t)sizeof(float);
-  return ng * kGroup - off_max - (kGroup - 1);
+  const int64_t ng = ((int64_t)lim - (int64_t)smem_bytes(0, 256)) / (int64_t)sizeof(float) + 1;
+  return ng * kGroup - (2 * kGroup - 1);
 }
 
 }  // extern "C"
