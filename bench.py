@@ -13,7 +13,9 @@ on).  Rows are independent, so under torchrun every rank samples its own batch
 ranks and `value` counts the rows of all ranks.
 
 Timing: W warm-up steps, then exactly K steps between a barrier and
-torch.cuda.synchronize(); CUDA events on the launching stream.  L2: the step
+torch.cuda.synchronize(), CUDA events on the launching stream.  The K steps are
+captured once into a CUDA graph (one kernel node per step) and replayed, so
+the device runs them back to back rather than waiting on Python.  L2: the step
 cycles through enough copies of the logits to exceed twice the 129 MB L2, so
 no step finds its inputs in L2.
 
@@ -248,38 +250,45 @@ def run_ours(args, world, rank, local):
         step(i, xs[i % copies])
     torch.cuda.synchronize()
 
-    # clocks: sample over a ~1 s soak of the same step loop that runs straight into the timed region
+    def capture(n_steps, first):
+        """One CUDA graph holding n_steps sampler launches (one kernel node per
+        step, each with its own Philox step), so the GPU runs them back to back
+        without waiting on the host."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for j in range(n_steps):
+                step(first + j, xs[j % copies])
+        return g
+
+    timed_graph = capture(args.steps, args.warmup)
+    soak_graph = capture(min(args.steps, 256), 0)
+    torch.cuda.synchronize()
+
+    # clocks: sample over a ~1 s soak of the same launches that runs straight into the timed region
     clk = ClockSampler(local)
     clk.start()
     t_soak = time.perf_counter()
-    i = 0
     while time.perf_counter() - t_soak < args.soak_s:
-        for _ in range(200):
-            step(i, xs[i % copies])
-            i += 1
+        soak_graph.replay()
         torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(args.warmup + i, xs[i % copies])
-        ends[i].record(stream)
+    timed_graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = clk.stop()
-    total_ms = t0.elapsed_time(t1)
-    kernel_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    total_ms = max_over_ranks(total_ms, world, device)
-    kernel_ms = max_over_ranks(kernel_ms, world, device)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, device)
+    # back-to-back graph launches: the mean launch duration is the region over K
+    # (it includes the few-hundred-ns gaps between kernel nodes)
+    kernel_ms = total_ms / args.steps
     ms_per_step = total_ms / args.steps
     rows_per_s = world * w.n * args.steps / (total_ms * 1e-3)
+    del timed_graph, soak_graph
 
     # end to end through the public API: pinned host inputs -> device, sample, ids -> host
     host_x = torch.from_numpy(w.logits.view(np.int16) if w.dtype == W.BF16 else w.logits).pin_memory()

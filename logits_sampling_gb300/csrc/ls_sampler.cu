@@ -21,6 +21,7 @@
 // host flags, log_probs_kernel) and the TokenSpeed "backends/triton.py" page
 // (TritonSamplingBackend: Gumbel-max sampling from per-request pools).
 
+#include <atomic>
 #include <cfloat>
 #include <cstdint>
 #include <cstdio>
@@ -104,14 +105,48 @@ struct RowView<bf16_tag> {
     off = (int)((a - reinterpret_cast<uintptr_t>(base)) / 2);
     V = vocab;
     NG = (int)((off + vocab + kGroup - 1) / kGroup);
+    g_full_lo = off > 0 ? 1 : 0;
+    g_full_hi = (int)((off + vocab) / kGroup) - 1;
   }
+  int g_full_lo, g_full_hi;  // groups lying entirely inside the row
   __device__ __forceinline__ int64_t index(int g, int e) const { return (int64_t)g * kGroup - off + e; }
   static constexpr int kWords = 8;
-  __device__ __forceinline__ float at(int64_t j) const { return bf16_bits_to_float(row[j]); }
-  __device__ __forceinline__ bool full(int g) const {
+  // Raw words of a group that straddles the row's ends; outside entries read as -inf.
+  __device__ __forceinline__ void load_words_partial(int g, uint32_t (&w)[kWords]) const {
     const int64_t j0 = index(g, 0);
-    return j0 >= 0 && j0 + kGroup <= V;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) {
+      const int64_t a = j0 + 2 * q, b = a + 1;
+      const uint32_t lo = (a >= 0 && a < V) ? (uint32_t)row[a] : 0xFF80u;
+      const uint32_t hi = (b >= 0 && b < V) ? (uint32_t)row[b] : 0xFF80u;
+      w[q] = lo | (hi << 16);
+    }
   }
+  // Maximum of the 16 entries (NaN ignored unless all are NaN).
+  __device__ __forceinline__ static float group_max(const uint32_t (&w)[kWords]) {
+    const uint32_t a = bmax2(bmax2(w[0], w[1]), bmax2(w[2], w[3]));
+    const uint32_t b = bmax2(bmax2(w[4], w[5]), bmax2(w[6], w[7]));
+    const uint32_t m = bmax2(a, b);
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  }
+  // Packed partial sums of 2^(v c - r) over the 16 entries.
+  __device__ __forceinline__ static f32x2 exp_sum(const uint32_t (&w)[kWords], f32x2 c2, f32x2 nr2) {
+    f32x2 s0 = 0ull, s1 = 0ull;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) {
+      const f32x2 t = fma2(pack2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u)), c2, nr2);
+      float t0, t1;
+      unpack2(t, t0, t1);
+      const f32x2 e = pack2(ex2(t0), ex2(t1));
+      if (q & 1)
+        s1 = add2(s1, e);
+      else
+        s0 = add2(s0, e);
+    }
+    return add2(s0, s1);
+  }
+  __device__ __forceinline__ float at(int64_t j) const { return bf16_bits_to_float(row[j]); }
+  __device__ __forceinline__ bool full(int g) const { return g >= g_full_lo && g <= g_full_hi; }
   __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords]) const { ld256(base + (size_t)g * 32, w); }
   __device__ __forceinline__ static void unpack(const uint32_t (&w)[kWords], float (&v)[kGroup]) {
 #pragma unroll
@@ -151,14 +186,45 @@ struct RowView<float> {
     off = (int)((a - reinterpret_cast<uintptr_t>(base)) / 4);
     V = vocab;
     NG = (int)((off + vocab + kGroup - 1) / kGroup);
+    g_full_lo = off > 0 ? 1 : 0;
+    g_full_hi = (int)((off + vocab) / kGroup) - 1;
   }
+  int g_full_lo, g_full_hi;  // groups lying entirely inside the row
   __device__ __forceinline__ int64_t index(int g, int e) const { return (int64_t)g * kGroup - off + e; }
   static constexpr int kWords = 16;
-  __device__ __forceinline__ float at(int64_t j) const { return row[j]; }
-  __device__ __forceinline__ bool full(int g) const {
+  __device__ __forceinline__ void load_words_partial(int g, uint32_t (&w)[kWords]) const {
     const int64_t j0 = index(g, 0);
-    return j0 >= 0 && j0 + kGroup <= V;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) {
+      const int64_t j = j0 + q;
+      w[q] = (j >= 0 && j < V) ? __float_as_uint(row[j]) : 0xFF800000u;
+    }
   }
+  __device__ __forceinline__ static float group_max(const uint32_t (&w)[kWords]) {
+    float v[kGroup];
+#pragma unroll
+    for (int q = 0; q < kGroup; ++q) v[q] = __uint_as_float(w[q]);
+    const float a = fmax3(v[0], v[1], v[2]), b = fmax3(v[3], v[4], v[5]), c = fmax3(v[6], v[7], v[8]);
+    const float d = fmax3(v[9], v[10], v[11]), e = fmax3(v[12], v[13], v[14]);
+    return fmaxf(fmax3(a, b, c), fmax3(d, e, v[15]));
+  }
+  __device__ __forceinline__ static f32x2 exp_sum(const uint32_t (&w)[kWords], f32x2 c2, f32x2 nr2) {
+    f32x2 s0 = 0ull, s1 = 0ull;
+#pragma unroll
+    for (int q = 0; q < kWords / 2; ++q) {
+      const f32x2 t = fma2(pack2(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1])), c2, nr2);
+      float t0, t1;
+      unpack2(t, t0, t1);
+      const f32x2 e = pack2(ex2(t0), ex2(t1));
+      if (q & 1)
+        s1 = add2(s1, e);
+      else
+        s0 = add2(s0, e);
+    }
+    return add2(s0, s1);
+  }
+  __device__ __forceinline__ float at(int64_t j) const { return row[j]; }
+  __device__ __forceinline__ bool full(int g) const { return g >= g_full_lo && g <= g_full_hi; }
   __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords]) const {
     ld256(base + (size_t)g * 64, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
     ld256(base + (size_t)g * 64 + 32, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
@@ -317,7 +383,7 @@ struct SelResult {
 // through rounding of a top-p target) the whole range is kept.
 template <typename TIn, bool kMass>
 __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo, uint32_t khi,
-                                  unsigned long long target, float joint_p, float M, float c) {
+                                  unsigned long long target, float joint_p, float R, float c) {
   using K = KeyOps<TIn>;
   unsigned long long above = 0, mass_at = 0;
   bool first = true;
@@ -334,7 +400,7 @@ __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo
       const uint32_t kk = K::key(v);
       if (v <= hi && kk >= base && kk <= top) {
         unsigned long long w = 1ull;
-        if (kMass) w = __float2ull_rn(exp2f((v - M) * c) * kMassScale);
+        if (kMass) w = __float2ull_rn(ex2(fmaf(v, c, -R)) * kMassScale);
         atomicAdd(&sh.hist[(kk - base) >> shift], w);
       }
     });
@@ -481,44 +547,38 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   rv.init(a.logits, src, a.stride, V);
 
   // ---- streaming pass: group maxima, running max, online mass ----------
-  float m = kNegInf, s = 0.f;
-  constexpr int U = RowView<TIn>::kBytes == 2 ? 4 : 2;
+  // Weights are 2^(v c - R) with c = log2(e) / T and R = RN(max * c): every
+  // mass in the row (total, candidate and kept masses) uses this one formula,
+  // so the rounding of R cancels in each ratio the cuts compare.  Each thread
+  // keeps its own reference r = RN(m c) for its running maximum m.
+  using RV = RowView<TIn>;
+  float m = kNegInf, r = 0.f;
+  f32x2 acc = 0ull;
+  const f32x2 c2 = pack2(c, c);
+  constexpr int U = RV::kBytes == 2 ? 4 : 2;
   for (int g0 = tid; g0 < rv.NG; g0 += kThreads * U) {
-    uint32_t w[U][RowView<TIn>::kWords];
+    uint32_t w[U][RV::kWords];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int g = g0 + u * kThreads;
-      if (g < rv.NG && rv.full(g)) rv.load_words(g, w[u]);
+      if (rv.full(g)) rv.load_words(g, w[u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int g = g0 + u * kThreads;
       if (g < rv.NG) {
-        float v[kGroup];
-        if (rv.full(g)) {
-          RowView<TIn>::unpack(w[u], v);
-        } else {
-          rv.load(g, v);
-        }
-        const float gm = max16(v);
+        if (!rv.full(g)) rv.load_words_partial(g, w[u]);
+        const float gm = RV::group_max(w[u]);
         gmax[g] = gm;
         if (need_sum) {
           if (gm > m) {
-            s *= exp2f((m - gm) * c);
+            const float rn = gm * c;
+            const float sc = ex2(r - rn);
+            acc = m > kNegInf ? mul2(acc, pack2(sc, sc)) : 0ull;
             m = gm;
+            r = rn;
           }
-          if (gm > kNegInf) {
-            // four interleaved partial sums of four terms each, then a tree
-            float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
-#pragma unroll
-            for (int q = 0; q < kGroup; q += 4) {
-              e0 += exp2f((v[q] - m) * c);
-              e1 += exp2f((v[q + 1] - m) * c);
-              e2 += exp2f((v[q + 2] - m) * c);
-              e3 += exp2f((v[q + 3] - m) * c);
-            }
-            s += (e0 + e1) + (e2 + e3);
-          }
+          if (gm > kNegInf) acc = add2(acc, RV::exp_sum(w[u], c2, pack2(-r, -r)));
         } else {
           m = fmaxf(m, gm);
         }
@@ -565,23 +625,26 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   }
 
   // ---- total mass (top-p without top-k, and unfiltered log-probs) -------
+  const float R = M * c;  // reference exponent of the row
   float S = 0.f;
   if (need_sum) {
-    const float st = m > kNegInf ? s * exp2f((m - M) * c) : 0.f;
+    float lo, hi;
+    unpack2(acc, lo, hi);
+    const float st = m > kNegInf ? (lo + hi) * ex2(r - R) : 0.f;
     S = block_reduce(st, OpAddF(), sh.red_f);
     if (!(S <= FLT_MAX)) {
       // A NaN entry poisoned the online sum: recompute it reading NaN as -inf.
-      float acc = 0.f;
+      float nacc = 0.f;
       for (int g = tid; g < rv.NG; g += kThreads) {
         float v[kGroup];
         rv.load(g, v);
 #pragma unroll
         for (int q = 0; q < kGroup; ++q) {
           const float x = v[q] == v[q] ? v[q] : kNegInf;
-          acc += exp2f((x - M) * c);
+          nacc += ex2(fmaf(x, c, -R));
         }
       }
-      S = block_reduce(acc, OpAddF(), sh.red_f);
+      S = block_reduce(nacc, OpAddF(), sh.red_f);
     }
   }
 
@@ -613,15 +676,15 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   uint32_t lo_key = K::key(-FLT_MAX);  // no filter: every finite entry
   unsigned long long kept_mass = 0ull;
   if (k_on) {
-    lo_key = radix_select<TIn, false>(sh, cs, K::key(lc), key_max, (unsigned long long)k, -1.f, M, c).key;
+    lo_key = radix_select<TIn, false>(sh, cs, K::key(lc), key_max, (unsigned long long)k, -1.f, R, c).key;
   }
   if (p_on) {
     SelResult r;
     if (k_on) {
-      r = radix_select<TIn, true>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), M, c);
+      r = radix_select<TIn, true>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), R, c);
     } else {
       const unsigned long long target = __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale);
-      r = radix_select<TIn, true>(sh, cs, K::key(lc), key_max, target, -1.f, M, c);
+      r = radix_select<TIn, true>(sh, cs, K::key(lc), key_max, target, -1.f, R, c);
     }
     lo_key = r.key;
     kept_mass = r.mass_ge;
@@ -644,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       lnS = logf(__ull2float_rn(kept_mass) / kMassScale);
     } else if (k_on) {
       cs.each(lo_val, [&](float v, int64_t) {
-        atomicAdd(&sh.acc, __float2ull_rn(exp2f((v - M) * c) * kMassScale));
+        atomicAdd(&sh.acc, __float2ull_rn(ex2(fmaf(v, c, -R)) * kMassScale));
       });
       __syncthreads();
       lnS = logf(__ull2float_rn(sh.acc) / kMassScale);
@@ -676,19 +739,29 @@ static int cand_capacity(int64_t vocab) {
   return cap;
 }
 
+constexpr int kMaxDevices = 64;
+
 static int max_dyn_smem() {
+  static std::atomic<int> cache[kMaxDevices];
   int dev = 0, v = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices && (v = cache[dev].load(std::memory_order_relaxed)) > 0) return v;
   if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
   return v;
 }
 
 template <typename TIn, int ROUTE, int MODE>
 static ls_status launch_rows(const KernelArgs& a, int32_t n, size_t smem, cudaStream_t stream) {
   auto kern = sampler_row_kernel<TIn, ROUTE, MODE>;
-  if (smem > 48 * 1024) {
+  // The dynamic shared-memory opt-in is set once per device and size class.
+  static std::atomic<size_t> opted[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LS_ERR_CUDA;
+  if (smem > 48 * 1024 && (dev < 0 || dev >= kMaxDevices || opted[dev].load(std::memory_order_relaxed) < smem)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return LS_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) opted[dev].store(smem, std::memory_order_relaxed);
   }
   kern<<<dim3((unsigned)n), dim3(kThreads), smem, stream>>>(a);
   return cudaPeekAtLastError() == cudaSuccess ? LS_OK : LS_ERR_CUDA;
