@@ -714,6 +714,9 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     } else {
       lnS = logf(S);
     }
+    // The masses are 2^(v c - R) = exp((v - M) / T) * 2^(M c - R); remove the
+    // exactly computable residual of R's rounding from the normaliser.
+    lnS -= fmaf(M, c, -R) * 0.6931471805599453f;
     write_row(rv, a.out_lp + i * V, [&](float v) { return v >= lo_val; },
               [&](float v) { return __fdiv_rn(v - M, T) - lnS; });
   }
