@@ -71,6 +71,10 @@ struct Shared {
   int cut_bin;
   int min_index;
   int cand_count;
+  int group_count;
+  float red_m[kWarps];
+  float red_s[kWarps];
+  float red_r[kWarps];
 };
 
 // ---------------------------------------------------------------------------
@@ -287,8 +291,8 @@ template <typename TIn>
 struct Cands {
   const RowView<TIn>* rv;
   const float* gmax;
-  const float* lv;
-  const int32_t* lj;
+  const float* lv;    // values
+  const int32_t* lj;  // vocabulary indices
   int count;
   bool listed;
   template <typename F>
@@ -304,35 +308,128 @@ struct Cands {
   }
 };
 
-// Copy the entries >= lo into the list; returns the candidate source.
+// Exclusive prefix sum of one int per thread (threadIdx order); *total gets
+// the block total.  Ends with the block synchronised.
+__device__ __forceinline__ int block_scan_int(Shared& sh, int v, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sh.red_i[w] = incl;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int q = 0; q < kWarps; ++q) {
+    const int x = sh.red_i[q];
+    base += q < w ? x : 0;
+    tot += x;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + incl - v;
+}
+
+// Build the candidate list of the entries >= lo, with block scans rather
+// than atomics so that no shared counter is contended:
+//  1. each thread counts the candidate groups (group maximum >= lo) among its
+//     groups in the shared-memory maxima; a scan places their indices in a
+//     group list (held in the histogram storage);
+//  2. candidate groups are loaded two per thread at a time (one L2 round trip
+//     per 1024 groups), and a scan of the per-thread entry counts places the
+//     entries >= lo in the list.
+// If either list would overflow, later phases re-read candidate groups from
+// global memory instead.
 template <typename TIn>
 __device__ Cands<TIn> collect_candidates(Shared& sh, const RowView<TIn>& rv, const float* gmax, float lo, float* lv,
                                          int32_t* lj, int cap) {
-  if (threadIdx.x == 0) sh.cand_count = 0;
+  int* gl = reinterpret_cast<int*>(sh.hist);
+  constexpr int kGroupCap = (int)(sizeof(sh.hist) / sizeof(int));
+  int mine = 0;
+  for (int g = threadIdx.x; g < rv.NG; g += kThreads) mine += gmax[g] >= lo ? 1 : 0;
+  int ngroups = 0;
+  int slot = block_scan_int(sh, mine, &ngroups);
+  if (ngroups > kGroupCap) return Cands<TIn>{&rv, gmax, lv, lj, 0, false};
+  for (int g = threadIdx.x; g < rv.NG; g += kThreads)
+    if (gmax[g] >= lo) gl[slot++] = g;
   __syncthreads();
-  for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
-    if (gmax[g] >= lo) {
-      float v[kGroup];
-      rv.load(g, v);
-      int cnt = 0;
+  int count = 0;
+  for (int c0 = 0; c0 < ngroups; c0 += 2 * kThreads) {
+    const int ca = c0 + threadIdx.x, cb = ca + kThreads;
+    float va[kGroup], vb[kGroup];
+    int ga = -1, gb = -1, cnt = 0;
+    if (ca < ngroups) {
+      ga = gl[ca];
+      rv.load(ga, va);
+    }
+    if (cb < ngroups) {
+      gb = gl[cb];
+      rv.load(gb, vb);
+    }
 #pragma unroll
-      for (int e = 0; e < kGroup; ++e) cnt += v[e] >= lo ? 1 : 0;
-      int slot = atomicAdd(&sh.cand_count, cnt);
+    for (int e = 0; e < kGroup; ++e) cnt += (ga >= 0 && va[e] >= lo ? 1 : 0) + (gb >= 0 && vb[e] >= lo ? 1 : 0);
+    int added = 0;
+    int at = count + block_scan_int(sh, cnt, &added);
 #pragma unroll
-      for (int e = 0; e < kGroup; ++e) {
-        if (v[e] >= lo) {
-          if (slot < cap) {
-            lv[slot] = v[e];
-            lj[slot] = (int32_t)rv.index(g, e);
-          }
-          ++slot;
+    for (int e = 0; e < kGroup; ++e) {
+      if (ga >= 0 && va[e] >= lo) {
+        if (at < cap) {
+          lv[at] = va[e];
+          lj[at] = (int32_t)rv.index(ga, e);
         }
+        ++at;
       }
     }
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e) {
+      if (gb >= 0 && vb[e] >= lo) {
+        if (at < cap) {
+          lv[at] = vb[e];
+          lj[at] = (int32_t)rv.index(gb, e);
+        }
+        ++at;
+      }
+    }
+    count += added;
   }
   __syncthreads();
-  const int count = sh.cand_count;
   return Cands<TIn>{&rv, gmax, lv, lj, count, count <= cap};
+}
+
+// Gumbel-max over the kept entries with value >= lo: id = argmax z + g,
+// z = v / T (z = 0 on a row whose maximum is +inf, `unit_z`).
+//  1. The maximum's ties (always kept) get exact scores; their best s_lb is a
+//     lower bound of the winner's score.
+//  2. Only entries with z >= s_lb - 16.6356 can still win (g <= 16.6356); of
+//     those, an entry needs g >= s_lb - z, i.e. u >= exp(-exp(z - s_lb)).
+//     That test (taken 1e-3 looser in g) runs on the Philox word alone, and
+//     only entries passing it compute the two logarithms.
+// Leaves the winner's key in sh.best (which must start at 0).
+template <typename TIn>
+__device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float lo, float T, bool unit_z,
+                              uint64_t seed, uint64_t step, uint32_t row) {
+  cs.each(M, [&](float v, int64_t j) {
+    const float z = unit_z ? 0.f : __fdiv_rn(v, T);
+    atomicMax(&sh.best, argmax_key(z + gumbel_of_word(noise_word(seed, step, row, j)), j));
+  });
+  __syncthreads();
+  if (unit_z) return;
+  const float s_lb = f32_from_key((uint32_t)(sh.best >> 32));
+  // z >= s_lb - 16.6356, in logit units (T > 0), lowered by a rounding margin
+  float lb = (s_lb - 16.6366f) * T;
+  lb -= fabsf(lb) * 1e-5f + 1e-30f;
+  cs.each(fmaxf(lo, lb), [&](float v, int64_t j) {
+    if (v >= M) return;
+    const float z = __fdiv_rn(v, T);
+    const float need = s_lb - z - 1e-3f;
+    const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
+    const uint32_t x = noise_word(seed, step, row, j);
+    const float u = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
+    if (u >= thr) atomicMax(&sh.best, argmax_key(z + gumbel_of_word(x), j));
+  });
+  __syncthreads();
 }
 
 // Find the highest bin b with above + sum_{b' >= b} hist[b'] >= target.  Writes
@@ -572,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
         gmax[g] = gm;
         if (need_sum) {
           if (gm > m) {
-            const float rn = gm * c;
+            const float rn = __fmul_rn(gm, c);  // rounded: never fused into r - rn
             const float sc = ex2(r - rn);
             acc = m > kNegInf ? mul2(acc, pack2(sc, sc)) : 0ull;
             m = gm;
@@ -585,10 +682,52 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       }
     }
   }
-  const float M = block_reduce(m, OpMax(), sh.red_f);  // NaN entries are ignored by fmaxf
+  // ---- row maximum and total mass in one block reduction -----------------
+  // Pairs (max, sum relative to RN(max * c)) combine like an online softmax.
+  const float m_thread = m;
+  float ssum = 0.f;
+  if (need_sum) {
+    float lo, hi;
+    unpack2(acc, lo, hi);
+    ssum = lo + hi;
+  }
+  {
+    float mw = m, sw = ssum, rw = r;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, mw, o);
+      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sw, o);
+      const float r2 = __shfl_xor_sync(0xFFFFFFFFu, rw, o);
+      const float mx = fmaxf(mw, m2);
+      if (need_sum && mx > kNegInf) {
+        const float rx = __fmul_rn(mx, c);
+        sw = (mw > kNegInf ? sw * ex2(rw - rx) : 0.f) + (m2 > kNegInf ? s2 * ex2(r2 - rx) : 0.f);
+        rw = rx;
+      }
+      mw = mx;
+    }
+    if ((tid & 31) == 0) {
+      sh.red_m[tid >> 5] = mw;
+      sh.red_s[tid >> 5] = sw;
+      sh.red_r[tid >> 5] = rw;
+    }
+  }
+  __syncthreads();
+  float M = kNegInf;
+#pragma unroll
+  for (int q = 0; q < kWarps; ++q) M = fmaxf(M, sh.red_m[q]);
   if (M == kNegInf) {
     row_error(a, i, MODE, LS_ROW_ERR_NO_FINITE);
     return;
+  }
+  const float R = __fmul_rn(M, c);  // reference exponent of the row (rounded product, never fused)
+  float S = 0.f;
+  if (need_sum && M < kPosInf) {
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) {
+      const float mq = sh.red_m[q];
+      if (mq > kNegInf) S += sh.red_s[q] * ex2(sh.red_r[q] - R);
+    }
   }
   if (tid == 0) {
     sh.best = 0ull;
@@ -596,25 +735,29 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     sh.min_index = 0x7FFFFFFF;
   }
   __syncthreads();
+  const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;
 
   // ---- rows without a temperature-scaled distribution -------------------
   // Greedy: the maximum's ties, lowest index.  +inf maximum: uniform over the
   // +inf entries (the limit of the softmax), i.e. Gumbel-max with z = 0 there.
   if (greedy || M == kPosInf) {
     const bool use_noise = !greedy;
-    const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;
     const Cands<TIn> cs = collect_candidates(sh, rv, gmax, M, cand_v, cand_j, a.cand_cap);
-    cs.each(M, [&](float, int64_t j) {
-      if (MODE == MODE_LOGPROBS) {
-        atomicAdd(&sh.acc, 1ull);
-      } else if (use_noise) {
-        const float sc = gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j));
-        atomicMax(&sh.best, argmax_key(sc, j));
-      } else {
-        atomicMin(&sh.min_index, (int)j);
-      }
-    });
-    __syncthreads();
+    if (MODE == MODE_SAMPLE && use_noise) {
+      gumbel_argmax(sh, cs, M, M, 1.f, true, seed, a.step, (uint32_t)i);
+    } else {
+      cs.each(M, [&](float, int64_t j) {
+        if (MODE == MODE_LOGPROBS) {
+          atomicAdd(&sh.acc, 1ull);
+        } else if (use_noise) {
+          const float sc = gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j));
+          atomicMax(&sh.best, argmax_key(sc, j));
+        } else {
+          atomicMin(&sh.min_index, (int)j);
+        }
+      });
+      __syncthreads();
+    }
     if (MODE == MODE_SAMPLE) {
       if (tid == 0) a.out_ids[i] = use_noise ? argmax_index(sh.best) : sh.min_index;
     } else {
@@ -624,28 +767,19 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     return;
   }
 
-  // ---- total mass (top-p without top-k, and unfiltered log-probs) -------
-  const float R = M * c;  // reference exponent of the row
-  float S = 0.f;
-  if (need_sum) {
-    float lo, hi;
-    unpack2(acc, lo, hi);
-    const float st = m > kNegInf ? (lo + hi) * ex2(r - R) : 0.f;
-    S = block_reduce(st, OpAddF(), sh.red_f);
-    if (!(S <= FLT_MAX)) {
-      // A NaN entry poisoned the online sum: recompute it reading NaN as -inf.
-      float nacc = 0.f;
-      for (int g = tid; g < rv.NG; g += kThreads) {
-        float v[kGroup];
-        rv.load(g, v);
+  // ---- total mass when a NaN entry poisoned the online sum ---------------
+  if (need_sum && !(S <= FLT_MAX)) {
+    float nacc = 0.f;
+    for (int g = tid; g < rv.NG; g += kThreads) {
+      float v[kGroup];
+      rv.load(g, v);
 #pragma unroll
-        for (int q = 0; q < kGroup; ++q) {
-          const float x = v[q] == v[q] ? v[q] : kNegInf;
-          nacc += ex2(fmaf(x, c, -R));
-        }
+      for (int q = 0; q < kGroup; ++q) {
+        const float x = v[q] == v[q] ? v[q] : kNegInf;
+        nacc += ex2(fmaf(x, c, -R));
       }
-      S = block_reduce(nacc, OpAddF(), sh.red_f);
     }
+    S = block_reduce(nacc, OpAddF(), sh.red_f);
   }
 
   // ---- candidate bound, candidate list ---------------------------------
@@ -658,19 +792,19 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   const uint32_t key_max = K::key(M);
   const float lg = M - kGumbelSpan * T;
   float lc = lg;
-  float gamma = kNegInf;
   if (k_on) {
-    gamma = thread_max_bound<TIn>(sh, m, k);
+    const float gamma = thread_max_bound<TIn>(sh, m_thread, k);
     lc = gamma > kNegInf ? gamma : -FLT_MAX;
   } else if (p_on) {
-    float Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
+    const float Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
     lc = fminf(fmaxf(Lp, -FLT_MAX), M);
   } else if (MODE == MODE_LOGPROBS) {
     lc = kPosInf;  // unfiltered log-probs need no candidates
   }
   lc = fmaxf(lc, -FLT_MAX);
-  const Cands<TIn> cs = (lc <= M) ? collect_candidates(sh, rv, gmax, lc, cand_v, cand_j, a.cand_cap)
-                                  : Cands<TIn>{&rv, gmax, cand_v, cand_j, 0, true};
+  const Cands<TIn> cs =
+      (lc <= M) ? collect_candidates(sh, rv, gmax, lc, cand_v, cand_j, a.cand_cap)
+                : Cands<TIn>{&rv, gmax, cand_v, cand_j, 0, true};
 
   // ---- exact top-k and top-p cuts ---------------------------------------
   uint32_t lo_key = K::key(-FLT_MAX);  // no filter: every finite entry
@@ -693,12 +827,9 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
 
   if (MODE == MODE_SAMPLE) {
     // ---- Gumbel-max over the kept set ------------------------------------
-    const uint64_t seed = a.seed[req];
-    cs.each(fmaxf(lo_val, lg), [&](float v, int64_t j) {
-      const float sc = __fdiv_rn(v, T) + gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j));
-      atomicMax(&sh.best, argmax_key(sc, j));
-    });
+    if (tid == 0) sh.best = 0ull;
     __syncthreads();
+    gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, false, seed, a.step, (uint32_t)i);
     if (tid == 0) a.out_ids[i] = argmax_index(sh.best);
   } else {
     // ---- log-probs of the processed distribution -------------------------
@@ -732,12 +863,12 @@ static size_t smem_bytes(int64_t vocab, int cap) {
   return sizeof(Shared) + (size_t)ng * sizeof(float) + (size_t)cap * (sizeof(float) + sizeof(int32_t));
 }
 
-// Candidate-list capacity: up to 4096 entries while two CTAs still fit on an
+// Candidate-list capacity: up to 8192 entries while two CTAs still fit on an
 // SM, never below 256.
 static int cand_capacity(int64_t vocab) {
   constexpr size_t kTwoPerSm = 112 * 1024;
   const size_t base = smem_bytes(vocab, 0);
-  int cap = 4096;
+  int cap = 8192;
   while (cap > 256 && base + (size_t)cap * 8 > kTwoPerSm) cap -= 256;
   return cap;
 }
