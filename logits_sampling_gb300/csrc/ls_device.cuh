@@ -15,6 +15,10 @@ constexpr int kGroup = 16;               // logits per group: one 32-byte sector
 constexpr int kBinBits = 11;
 constexpr int kBins = 1 << kBinBits;     // bins per radix-select level
 constexpr int kBinsPerThread = kBins / kThreads;
+// The first select level is built while collecting candidates, with four
+// sub-counters per bin (lane mod 4) against atomic contention: 512 bins.
+constexpr int kBinBits1 = 9;
+static_assert((1 << kBinBits1) * 4 == kBins && (1 << kBinBits1) <= kThreads, "first-level bins");
 static_assert(kBins % kThreads == 0, "bins must split evenly over threads");
 
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -152,6 +156,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+// take ? cand : cur, opaque to the compiler so that a chain of these over a
+// register array is not turned back into (local-memory) indexing.
+__device__ __forceinline__ uint32_t select_word(uint32_t cur, uint32_t cand, bool take) {
+  uint32_t r;
+  asm("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %3, 0;\n\tselp.b32 %0, %1, %2, p;\n\t}"
+      : "=r"(r)
+      : "r"(cand), "r"(cur), "r"((uint32_t)take));
+  return r;
+}
+
 // 2^x with results below 2^-126 flushed to zero (they are far below the
 // resolution of any sum here).
 __device__ __forceinline__ float ex2(float x) {

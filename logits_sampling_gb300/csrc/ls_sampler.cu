@@ -60,22 +60,37 @@ struct KernelArgs {
 
 // Fixed part of the dynamic shared memory; the group maxima follow it.
 struct Shared {
-  unsigned long long hist[kBins];
+  // Histogram: u32 counts, or masses as (lo, hi) u32 pairs updated with
+  // carry-propagating 32-bit atomics (shared-memory 64-bit adds are not
+  // native and degrade badly under contention).
+  unsigned int hist[2 * kBins];
   unsigned long long red_u64[kWarps];
   float red_f[kWarps];
   int red_i[kWarps];
   unsigned long long best;
-  unsigned long long acc;
+  unsigned int acc[2];  // a count in acc[0], or a mass as a (lo, hi) pair
   unsigned long long cut_above;
   unsigned long long cut_mass;
   int cut_bin;
   int min_index;
   int cand_count;
-  int group_count;
   float red_m[kWarps];
   float red_s[kWarps];
   float red_r[kWarps];
 };
+
+// Exact 64-bit add into a (lo, hi) pair of u32 counters with two native
+// 32-bit atomics: the thread whose addition wraps the low word carries one
+// into the high word, so the pair ends at the exact sum in any order.
+__device__ __forceinline__ void add_mass(unsigned int* pair, unsigned long long w) {
+  const unsigned int lo = (unsigned int)w, hi = (unsigned int)(w >> 32);
+  const unsigned int old = atomicAdd(pair, lo);
+  const unsigned int carry = (old + lo < old) ? 1u : 0u;
+  if (hi + carry) atomicAdd(pair + 1, hi + carry);
+}
+__device__ __forceinline__ unsigned long long read_mass(const unsigned int* pair) {
+  return ((unsigned long long)pair[1] << 32) | pair[0];
+}
 
 // ---------------------------------------------------------------------------
 // Row view: groups of 16 logits aligned to the group size in bytes, so that
@@ -132,6 +147,23 @@ struct RowView<bf16_tag> {
     const uint32_t b = bmax2(bmax2(w[4], w[5]), bmax2(w[6], w[7]));
     const uint32_t m = bmax2(a, b);
     return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  }
+  // Bit e set when entry e is >= lo (NaN never).
+  __device__ __forceinline__ static uint32_t ge_mask(const uint32_t (&w)[kWords], float lo) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) {
+      m |= (__uint_as_float(w[q] << 16) >= lo ? 1u : 0u) << (2 * q);
+      m |= (__uint_as_float(w[q] & 0xFFFF0000u) >= lo ? 1u : 0u) << (2 * q + 1);
+    }
+    return m;
+  }
+  // Entry e of the group (a select chain, so the words stay in registers).
+  __device__ __forceinline__ static float element(const uint32_t (&w)[kWords], int e) {
+    uint32_t word = w[0];
+#pragma unroll
+    for (int q = 1; q < kWords; ++q) word = select_word(word, w[q], (e >> 1) == q);
+    return __uint_as_float((e & 1) ? (word & 0xFFFF0000u) : (word << 16));
   }
   // Packed partial sums of 2^(v c - r) over the 16 entries.
   __device__ __forceinline__ static f32x2 exp_sum(const uint32_t (&w)[kWords], f32x2 c2, f32x2 nr2) {
@@ -211,6 +243,18 @@ struct RowView<float> {
     const float a = fmax3(v[0], v[1], v[2]), b = fmax3(v[3], v[4], v[5]), c = fmax3(v[6], v[7], v[8]);
     const float d = fmax3(v[9], v[10], v[11]), e = fmax3(v[12], v[13], v[14]);
     return fmaxf(fmax3(a, b, c), fmax3(d, e, v[15]));
+  }
+  __device__ __forceinline__ static uint32_t ge_mask(const uint32_t (&w)[kWords], float lo) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) m |= (__uint_as_float(w[q]) >= lo ? 1u : 0u) << q;
+    return m;
+  }
+  __device__ __forceinline__ static float element(const uint32_t (&w)[kWords], int e) {
+    uint32_t word = w[0];
+#pragma unroll
+    for (int q = 1; q < kWords; ++q) word = select_word(word, w[q], e == q);
+    return __uint_as_float(word);
   }
   __device__ __forceinline__ static f32x2 exp_sum(const uint32_t (&w)[kWords], f32x2 c2, f32x2 nr2) {
     f32x2 s0 = 0ull, s1 = 0ull;
@@ -308,114 +352,16 @@ struct Cands {
   }
 };
 
-// Exclusive prefix sum of one int per thread (threadIdx order); *total gets
-// the block total.  Ends with the block synchronised.
-__device__ __forceinline__ int block_scan_int(Shared& sh, int v, int* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) sh.red_i[w] = incl;
-  __syncthreads();
-  int base = 0, tot = 0;
-#pragma unroll
-  for (int q = 0; q < kWarps; ++q) {
-    const int x = sh.red_i[q];
-    base += q < w ? x : 0;
-    tot += x;
-  }
-  __syncthreads();
-  *total = tot;
-  return base + incl - v;
-}
-
-// Build the candidate list of the entries >= lo, with block scans rather
-// than atomics so that no shared counter is contended:
-//  1. each thread counts the candidate groups (group maximum >= lo) among its
-//     groups in the shared-memory maxima; a scan places their indices in a
-//     group list (held in the histogram storage);
-//  2. candidate groups are loaded two per thread at a time (one L2 round trip
-//     per 1024 groups), and a scan of the per-thread entry counts places the
-//     entries >= lo in the list.
-// If either list would overflow, later phases re-read candidate groups from
-// global memory instead.
+// Gumbel-max over the kept entries with value >= lo, given in sh.best the
+// exact score of the best of the maximum's ties (always kept): s_lb, a lower
+// bound of the winner's score.  Only entries with z >= s_lb - 16.6356 can
+// still win (g <= 16.6356); of those, an entry needs g >= s_lb - z, i.e.
+// u >= exp(-exp(z - s_lb)).  That test (taken 1e-3 looser in g) runs on the
+// Philox word alone, and only entries passing it compute the two logarithms.
+// Leaves the winner's key in sh.best.
 template <typename TIn>
-__device__ Cands<TIn> collect_candidates(Shared& sh, const RowView<TIn>& rv, const float* gmax, float lo, float* lv,
-                                         int32_t* lj, int cap) {
-  int* gl = reinterpret_cast<int*>(sh.hist);
-  constexpr int kGroupCap = (int)(sizeof(sh.hist) / sizeof(int));
-  int mine = 0;
-  for (int g = threadIdx.x; g < rv.NG; g += kThreads) mine += gmax[g] >= lo ? 1 : 0;
-  int ngroups = 0;
-  int slot = block_scan_int(sh, mine, &ngroups);
-  if (ngroups > kGroupCap) return Cands<TIn>{&rv, gmax, lv, lj, 0, false};
-  for (int g = threadIdx.x; g < rv.NG; g += kThreads)
-    if (gmax[g] >= lo) gl[slot++] = g;
-  __syncthreads();
-  int count = 0;
-  for (int c0 = 0; c0 < ngroups; c0 += 2 * kThreads) {
-    const int ca = c0 + threadIdx.x, cb = ca + kThreads;
-    float va[kGroup], vb[kGroup];
-    int ga = -1, gb = -1, cnt = 0;
-    if (ca < ngroups) {
-      ga = gl[ca];
-      rv.load(ga, va);
-    }
-    if (cb < ngroups) {
-      gb = gl[cb];
-      rv.load(gb, vb);
-    }
-#pragma unroll
-    for (int e = 0; e < kGroup; ++e) cnt += (ga >= 0 && va[e] >= lo ? 1 : 0) + (gb >= 0 && vb[e] >= lo ? 1 : 0);
-    int added = 0;
-    int at = count + block_scan_int(sh, cnt, &added);
-#pragma unroll
-    for (int e = 0; e < kGroup; ++e) {
-      if (ga >= 0 && va[e] >= lo) {
-        if (at < cap) {
-          lv[at] = va[e];
-          lj[at] = (int32_t)rv.index(ga, e);
-        }
-        ++at;
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < kGroup; ++e) {
-      if (gb >= 0 && vb[e] >= lo) {
-        if (at < cap) {
-          lv[at] = vb[e];
-          lj[at] = (int32_t)rv.index(gb, e);
-        }
-        ++at;
-      }
-    }
-    count += added;
-  }
-  __syncthreads();
-  return Cands<TIn>{&rv, gmax, lv, lj, count, count <= cap};
-}
-
-// Gumbel-max over the kept entries with value >= lo: id = argmax z + g,
-// z = v / T (z = 0 on a row whose maximum is +inf, `unit_z`).
-//  1. The maximum's ties (always kept) get exact scores; their best s_lb is a
-//     lower bound of the winner's score.
-//  2. Only entries with z >= s_lb - 16.6356 can still win (g <= 16.6356); of
-//     those, an entry needs g >= s_lb - z, i.e. u >= exp(-exp(z - s_lb)).
-//     That test (taken 1e-3 looser in g) runs on the Philox word alone, and
-//     only entries passing it compute the two logarithms.
-// Leaves the winner's key in sh.best (which must start at 0).
-template <typename TIn>
-__device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float lo, float T, bool unit_z,
-                              uint64_t seed, uint64_t step, uint32_t row) {
-  cs.each(M, [&](float v, int64_t j) {
-    const float z = unit_z ? 0.f : __fdiv_rn(v, T);
-    atomicMax(&sh.best, argmax_key(z + gumbel_of_word(noise_word(seed, step, row, j)), j));
-  });
-  __syncthreads();
-  if (unit_z) return;
+__device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float lo, float T, uint64_t seed,
+                              uint64_t step, uint32_t row) {
   const float s_lb = f32_from_key((uint32_t)(sh.best >> 32));
   // z >= s_lb - 16.6356, in logit units (T > 0), lowered by a rounding margin
   float lb = (s_lb - 16.6366f) * T;
@@ -435,6 +381,12 @@ __device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float l
 // Find the highest bin b with above + sum_{b' >= b} hist[b'] >= target.  Writes
 // sh.cut_bin (-1 when the total never reaches target), sh.cut_above (weight
 // strictly above bin b, including `above`) and sh.cut_mass (hist[b]).
+template <bool kMass>
+__device__ __forceinline__ unsigned long long bin_weight(const Shared& sh, int b) {
+  return kMass ? read_mass(&sh.hist[2 * b]) : (unsigned long long)sh.hist[b];
+}
+
+template <bool kMass>
 __device__ __forceinline__ void find_cut_bin(Shared& sh, int nb, unsigned long long above, unsigned long long target) {
   const int t = threadIdx.x;
   const int top = nb - 1 - t * kBinsPerThread;
@@ -442,7 +394,7 @@ __device__ __forceinline__ void find_cut_bin(Shared& sh, int nb, unsigned long l
 #pragma unroll
   for (int q = 0; q < kBinsPerThread; ++q) {
     const int b = top - q;
-    if (b >= 0) local += sh.hist[b];
+    if (b >= 0) local += bin_weight<kMass>(sh, b);
   }
   if (t == 0) sh.cut_bin = -1;
   unsigned long long cum = above + block_exclusive_scan(local, sh.red_u64);
@@ -451,7 +403,7 @@ __device__ __forceinline__ void find_cut_bin(Shared& sh, int nb, unsigned long l
     for (int q = 0; q < kBinsPerThread; ++q) {
       const int b = top - q;
       if (b < 0) break;
-      const unsigned long long h = sh.hist[b];
+      const unsigned long long h = bin_weight<kMass>(sh, b);
       if (cum + h >= target) {
         sh.cut_bin = b;
         sh.cut_above = cum;
@@ -469,9 +421,9 @@ struct SelResult {
   unsigned long long mass_ge;   // weight of the kept entries
 };
 
-// Exact threshold select over the row entries with keys in [klo, khi]:
-// returns the largest key kappa such that (weight of entries with key in
-// [kappa, khi]) >= target, where weight is 1 (top-k, target = k) or the
+// Exact threshold select over the row entries with keys in [klo, khi], given
+// the weight `above` of the entries with larger keys: returns the largest key
+// kappa such that above + (weight of entries with key in [kappa, khi]) >= target, where weight is 1 (top-k, target = k) or the
 // fixed-point probability mass exp((l - M)/T) * 2^40 (top-p).  With
 // joint_p >= 0 the target is joint_p * (total weight of the range), taken from
 // the first level's histogram.  Each level splits the remaining key range into
@@ -480,42 +432,45 @@ struct SelResult {
 // through rounding of a top-p target) the whole range is kept.
 template <typename TIn, bool kMass>
 __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo, uint32_t khi,
-                                  unsigned long long target, float joint_p, float R, float c) {
+                                  unsigned long long target, float joint_p, float R, float c,
+                                  unsigned long long above) {
   using K = KeyOps<TIn>;
-  unsigned long long above = 0, mass_at = 0;
+  unsigned long long mass_at = 0;
   bool first = true;
   do {
     const uint32_t width = khi - klo;
     const int bits = width ? 32 - __clz(width) : 0;
     const int shift = bits > kBinBits ? bits - kBinBits : 0;
     const int nb = (int)(width >> shift) + 1;
-    for (int b = threadIdx.x; b < nb; b += kThreads) sh.hist[b] = 0ull;
+    for (int b = threadIdx.x; b < (kMass ? 2 * nb : nb); b += kThreads) sh.hist[b] = 0u;
     __syncthreads();
     const float lo = K::value(klo), hi = K::value(khi);
     const uint32_t base = klo, top = khi;
     cs.each(lo, [&](float v, int64_t) {
       const uint32_t kk = K::key(v);
       if (v <= hi && kk >= base && kk <= top) {
-        unsigned long long w = 1ull;
-        if (kMass) w = __float2ull_rn(ex2(fmaf(v, c, -R)) * kMassScale);
-        atomicAdd(&sh.hist[(kk - base) >> shift], w);
+        const int bin = (int)((kk - base) >> shift);
+        if (kMass)
+          add_mass(&sh.hist[2 * bin], __float2ull_rn(ex2(fmaf(v, c, -R)) * kMassScale));
+        else
+          atomicAdd(&sh.hist[bin], 1u);
       }
     });
     __syncthreads();
     if (first && joint_p >= 0.f) {
       unsigned long long part = 0;
-      for (int b = threadIdx.x; b < nb; b += kThreads) part += sh.hist[b];
+      for (int b = threadIdx.x; b < nb; b += kThreads) part += bin_weight<kMass>(sh, b);
       const unsigned long long total = block_reduce(part, OpAddU64(), sh.red_u64);
       target = __float2ull_ru(joint_p * __ull2float_rn(total));
     }
     if (target < 1ull) target = 1ull;
-    find_cut_bin(sh, nb, above, target);
+    find_cut_bin<kMass>(sh, nb, above, target);
     const int b = sh.cut_bin;
     if (b < 0) {  // only reachable on the first level
       unsigned long long part = 0;
-      for (int q = threadIdx.x; q < nb; q += kThreads) part += sh.hist[q];
+      for (int q = threadIdx.x; q < nb; q += kThreads) part += bin_weight<kMass>(sh, q);
       const unsigned long long total = block_reduce(part, OpAddU64(), sh.red_u64);
-      return SelResult{klo, total};
+      return SelResult{klo, above + total};
     }
     above = sh.cut_above;
     mass_at = sh.cut_mass;
@@ -527,33 +482,6 @@ __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo
     __syncthreads();
   } while (klo < khi);
   return SelResult{klo, above + mass_at};
-}
-
-// A value gamma such that at least k of the threads' running maxima are
-// >= gamma (hence at least k row entries are), within one histogram bin of the
-// k-th largest thread maximum; -inf when fewer than k threads saw a finite
-// entry.  It bounds the top-k cut from below.
-template <typename TIn>
-__device__ float thread_max_bound(Shared& sh, float m, int k) {
-  using K = KeyOps<TIn>;
-  const bool fin = m > kNegInf;
-  const int F = block_reduce(fin ? 1 : 0, OpAddI(), sh.red_i);
-  if (F < k) return kNegInf;
-  const float mn = block_reduce(fin ? m : kPosInf, OpMin(), sh.red_f);
-  const float mx = block_reduce(m, OpMax(), sh.red_f);
-  const uint32_t klo = K::key(mn), khi = K::key(mx);
-  const uint32_t width = khi - klo;
-  const int bits = width ? 32 - __clz(width) : 0;
-  const int shift = bits > kBinBits ? bits - kBinBits : 0;
-  const int nb = (int)(width >> shift) + 1;
-  for (int b = threadIdx.x; b < nb; b += kThreads) sh.hist[b] = 0ull;
-  __syncthreads();
-  if (fin) atomicAdd(&sh.hist[(K::key(m) - klo) >> shift], 1ull);
-  __syncthreads();
-  find_cut_bin(sh, nb, 0ull, (unsigned long long)k);
-  const int b = sh.cut_bin;
-  __syncthreads();
-  return b < 0 ? kNegInf : K::value(klo + ((uint32_t)b << shift));
 }
 
 __device__ __forceinline__ void row_error(const KernelArgs& a, int64_t i, int mode, int err) {
@@ -682,17 +610,20 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       }
     }
   }
-  // ---- row maximum and total mass in one block reduction -----------------
-  // Pairs (max, sum relative to RN(max * c)) combine like an online softmax.
-  const float m_thread = m;
-  float ssum = 0.f;
-  if (need_sum) {
-    float lo, hi;
-    unpack2(acc, lo, hi);
-    ssum = lo + hi;
-  }
+  // ---- one block reduction: row maximum, total mass, top-k bound --------
+  // (max, sum relative to RN(max * c)) pairs combine like an online softmax.
+  // For a top-k row each warp also extracts the j-th largest of its 32 thread
+  // maxima, j = ceil(k / 16): all 16 warps then hold >= j thread maxima (hence
+  // >= k distinct entries) at or above the smallest of those, gamma.
+  for (int q = tid; q < 2 * kBins; q += kThreads) sh.hist[q] = 0u;  // first-level histogram
+  const int lane = tid & 31;
   {
-    float mw = m, sw = ssum, rw = r;
+    float mw = m, sw = 0.f, rw = r;
+    if (need_sum) {
+      float lo, hi;
+      unpack2(acc, lo, hi);
+      sw = lo + hi;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xFFFFFFFFu, mw, o);
@@ -706,16 +637,37 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       }
       mw = mx;
     }
-    if ((tid & 31) == 0) {
+    float gj = kNegInf;
+    if (k_on && k <= 32 * kWarps) {
+      const int jrank = (k + kWarps - 1) / kWarps;
+      float cur = m;
+      for (int t = 0; t < jrank; ++t) {
+        gj = warp_reduce(cur, OpMax());
+        const unsigned holders = __ballot_sync(0xFFFFFFFFu, cur == gj);
+        if (lane == __ffs(holders) - 1) cur = kNegInf;
+      }
+    }
+    if (lane == 0) {
       sh.red_m[tid >> 5] = mw;
       sh.red_s[tid >> 5] = sw;
       sh.red_r[tid >> 5] = rw;
+      sh.red_f[tid >> 5] = gj;
     }
   }
+  if (tid == 0) {
+    sh.best = 0ull;
+    sh.acc[0] = 0u;
+    sh.acc[1] = 0u;
+    sh.min_index = 0x7FFFFFFF;
+    sh.cand_count = 0;
+  }
   __syncthreads();
-  float M = kNegInf;
+  float M = kNegInf, gamma = kPosInf;
 #pragma unroll
-  for (int q = 0; q < kWarps; ++q) M = fmaxf(M, sh.red_m[q]);
+  for (int q = 0; q < kWarps; ++q) {
+    M = fmaxf(M, sh.red_m[q]);
+    gamma = fminf(gamma, sh.red_f[q]);
+  }
   if (M == kNegInf) {
     row_error(a, i, MODE, LS_ROW_ERR_NO_FINITE);
     return;
@@ -729,46 +681,11 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       if (mq > kNegInf) S += sh.red_s[q] * ex2(sh.red_r[q] - R);
     }
   }
-  if (tid == 0) {
-    sh.best = 0ull;
-    sh.acc = 0ull;
-    sh.min_index = 0x7FFFFFFF;
-  }
-  __syncthreads();
   const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;
-
-  // ---- rows without a temperature-scaled distribution -------------------
-  // Greedy: the maximum's ties, lowest index.  +inf maximum: uniform over the
-  // +inf entries (the limit of the softmax), i.e. Gumbel-max with z = 0 there.
-  if (greedy || M == kPosInf) {
-    const bool use_noise = !greedy;
-    const Cands<TIn> cs = collect_candidates(sh, rv, gmax, M, cand_v, cand_j, a.cand_cap);
-    if (MODE == MODE_SAMPLE && use_noise) {
-      gumbel_argmax(sh, cs, M, M, 1.f, true, seed, a.step, (uint32_t)i);
-    } else {
-      cs.each(M, [&](float, int64_t j) {
-        if (MODE == MODE_LOGPROBS) {
-          atomicAdd(&sh.acc, 1ull);
-        } else if (use_noise) {
-          const float sc = gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j));
-          atomicMax(&sh.best, argmax_key(sc, j));
-        } else {
-          atomicMin(&sh.min_index, (int)j);
-        }
-      });
-      __syncthreads();
-    }
-    if (MODE == MODE_SAMPLE) {
-      if (tid == 0) a.out_ids[i] = use_noise ? argmax_index(sh.best) : sh.min_index;
-    } else {
-      const float lp = -logf((float)sh.acc);
-      write_row(rv, a.out_lp + i * V, [&](float v) { return v >= M; }, [&](float) { return lp; });
-    }
-    return;
-  }
+  const bool tie_only = greedy || M == kPosInf;  // no temperature-scaled distribution
 
   // ---- total mass when a NaN entry poisoned the online sum ---------------
-  if (need_sum && !(S <= FLT_MAX)) {
+  if (!tie_only && need_sum && !(S <= FLT_MAX)) {
     float nacc = 0.f;
     for (int g = tid; g < rv.NG; g += kThreads) {
       float v[kGroup];
@@ -782,54 +699,200 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     S = block_reduce(nacc, OpAddF(), sh.red_f);
   }
 
-  // ---- candidate bound, candidate list ---------------------------------
-  // Every entry that any later phase needs is >= lc:
-  //  * top-k: at least k thread maxima (hence k entries) are >= gamma;
+  // ---- candidate bound --------------------------------------------------
+  // Every entry that a later phase needs is >= lc:
+  //  * ties-only rows (greedy, +inf maximum): the maximum itself;
+  //  * top-k: gamma (at least k entries are >= gamma);
   //  * top-p alone: the entries below Lp carry less than (1 - p) S e^-2, so
   //    the cut lies above Lp;
   //  * no filter: an entry with z more than the noise span below max z can
   //    never beat the maximum's perturbed score.
-  const uint32_t key_max = K::key(M);
   const float lg = M - kGumbelSpan * T;
-  float lc = lg;
-  if (k_on) {
-    const float gamma = thread_max_bound<TIn>(sh, m_thread, k);
+  float lc;
+  int kind = 0;  // first-level histogram: 0 none, 1 count (top-k), 2 mass (top-p alone)
+  if (tie_only) {
+    lc = M;
+  } else if (k_on) {
     lc = gamma > kNegInf ? gamma : -FLT_MAX;
+    kind = 1;
   } else if (p_on) {
     const float Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
     lc = fminf(fmaxf(Lp, -FLT_MAX), M);
-  } else if (MODE == MODE_LOGPROBS) {
-    lc = kPosInf;  // unfiltered log-probs need no candidates
+    kind = 2;
+  } else {
+    lc = MODE == MODE_LOGPROBS ? kPosInf : lg;  // unfiltered log-probs need no candidates
   }
   lc = fmaxf(lc, -FLT_MAX);
-  const Cands<TIn> cs =
-      (lc <= M) ? collect_candidates(sh, rv, gmax, lc, cand_v, cand_j, a.cand_cap)
-                : Cands<TIn>{&rv, gmax, cand_v, cand_j, 0, true};
+  const uint32_t key_max = K::key(M);
+  const uint32_t klo1 = K::key(lc);
+  const uint32_t width1 = key_max - klo1;
+  const int bits1 = width1 ? 32 - __clz(width1) : 0;
+  const int shift1 = bits1 > kBinBits1 ? bits1 - kBinBits1 : 0;
+  const int nb1 = (int)(width1 >> shift1) + 1;
+
+  // ---- collect: each thread loads its own candidate groups --------------
+  // A thread wrote the maxima of groups tid, tid + 512, ...; the candidate
+  // ones (maximum >= lc) are loaded a few at a time with all loads in flight
+  // at once.  Their entries >= lc are appended to the shared-memory list (one
+  // warp-aggregated atomic per warp and round) and feed the first select
+  // level's histogram (4 sub-counters per bin against contention).
+  using RVT = RowView<TIn>;
+  constexpr int GPR = RVT::kBytes == 2 ? 4 : 2;  // groups loaded per round
+  int count = 0;
+  if (lc <= M) {
+    const int slots = (rv.NG + kThreads - 1) / kThreads;
+    for (int sbase = 0; sbase < slots; sbase += 32) {
+      uint32_t mask = 0u;
+      const int send = min(slots, sbase + 32);
+      for (int sl = sbase; sl < send; ++sl) {
+        const int g = tid + sl * kThreads;
+        if (g < rv.NG && gmax[g] >= lc) mask |= 1u << (sl - sbase);
+      }
+      const int rounds = __reduce_max_sync(0xFFFFFFFFu, (__popc(mask) + GPR - 1) / GPR);
+      for (int rd = 0; rd < rounds; ++rd) {
+        uint32_t w[GPR][RVT::kWords];
+        int gg[GPR];
+#pragma unroll
+        for (int u = 0; u < GPR; ++u) {
+          gg[u] = -1;
+          if (mask) {
+            const int sl = __ffs(mask) - 1;
+            mask &= mask - 1u;
+            gg[u] = tid + (sbase + sl) * kThreads;
+            if (rv.full(gg[u])) rv.load_words(gg[u], w[u]);
+          }
+        }
+        uint32_t em[GPR];
+        int cnt = 0;
+#pragma unroll
+        for (int u = 0; u < GPR; ++u) {
+          em[u] = 0u;
+          if (gg[u] >= 0) {
+            if (!rv.full(gg[u])) rv.load_words_partial(gg[u], w[u]);
+            em[u] = RVT::ge_mask(w[u], lc);
+            cnt += __popc(em[u]);
+          }
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t2;
+        }
+        int base = 0;
+        if (lane == 31) base = atomicAdd(&sh.cand_count, incl);
+        int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll
+        for (int u = 0; u < GPR; ++u) {
+          uint32_t mm = em[u];
+#pragma unroll 1
+          while (mm) {
+            const int e = __ffs(mm) - 1;
+            mm &= mm - 1u;
+            const float x = RVT::element(w[u], e);
+            if (at < a.cand_cap) {
+              cand_v[at] = x;
+              cand_j[at] = (int32_t)rv.index(gg[u], e);
+            }
+            ++at;
+            if (kind != 0) {
+              const uint32_t kk = K::key(x);
+              if (kk >= klo1 && kk <= key_max) {
+                const int sub = (int)(((kk - klo1) >> shift1) << 2) | (lane & 3);
+                if (kind == 2)
+                  add_mass(&sh.hist[2 * sub], __float2ull_rn(ex2(fmaf(x, c, -R)) * kMassScale));
+                else
+                  atomicAdd(&sh.hist[sub], 1u);
+              }
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    count = sh.cand_count;
+  }
+  const Cands<TIn> cs{&rv, gmax, cand_v, cand_j, count, count <= a.cand_cap};
+
+  // The maximum's ties: lowest index (greedy), count (log-probs of ties-only
+  // rows) or exact Gumbel score (sampling; the best is a lower bound of the
+  // winner's score).
+  if (lc <= M && (MODE == MODE_SAMPLE || tie_only)) {
+    cs.each(M, [&](float x, int64_t j) {
+      if (MODE == MODE_LOGPROBS) {
+        atomicAdd(&sh.acc[0], 1u);
+      } else if (greedy) {
+        atomicMin(&sh.min_index, (int)j);
+      } else {
+        const float z = M == kPosInf ? 0.f : __fdiv_rn(x, T);
+        atomicMax(&sh.best, argmax_key(z + gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j)), j));
+      }
+    });
+    __syncthreads();
+  }
+  if (tie_only) {
+    if (MODE == MODE_SAMPLE) {
+      if (tid == 0) a.out_ids[i] = greedy ? sh.min_index : argmax_index(sh.best);
+    } else {
+      const float lp = -logf((float)sh.acc[0]);
+      write_row(rv, a.out_lp + i * V, [&](float v) { return v >= M; }, [&](float) { return lp; });
+    }
+    return;
+  }
 
   // ---- exact top-k and top-p cuts ---------------------------------------
   uint32_t lo_key = K::key(-FLT_MAX);  // no filter: every finite entry
   unsigned long long kept_mass = 0ull;
-  if (k_on) {
-    lo_key = radix_select<TIn, false>(sh, cs, K::key(lc), key_max, (unsigned long long)k, -1.f, R, c).key;
-  }
-  if (p_on) {
-    SelResult r;
-    if (k_on) {
-      r = radix_select<TIn, true>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), R, c);
-    } else {
-      const unsigned long long target = __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale);
-      r = radix_select<TIn, true>(sh, cs, K::key(lc), key_max, target, -1.f, R, c);
+  if (kind != 0) {
+    // first level from the histogram built while collecting: one bin per
+    // thread, scanned from the highest bin down
+    const unsigned long long target =
+        kind == 1 ? (unsigned long long)k : max(1ull, __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale));
+    unsigned long long h = 0ull;
+    const int b = nb1 - 1 - tid;
+    if (b >= 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        h += kind == 2 ? read_mass(&sh.hist[2 * (4 * b + q)]) : (unsigned long long)sh.hist[4 * b + q];
     }
-    lo_key = r.key;
-    kept_mass = r.mass_ge;
+    if (tid == 0) sh.cut_bin = -1;
+    const unsigned long long cum = block_exclusive_scan(h, sh.red_u64);
+    if (b >= 0 && cum < target && cum + h >= target) {
+      sh.cut_bin = b;
+      sh.cut_above = cum;
+      sh.cut_mass = h;
+    }
+    __syncthreads();
+    SelResult r1;
+    if (sh.cut_bin < 0) {  // only through rounding of a top-p target: keep every candidate
+      const unsigned long long part = b >= 0 ? h : 0ull;
+      r1 = SelResult{klo1, block_reduce(part, OpAddU64(), sh.red_u64)};
+    } else {
+      const uint32_t nlo = klo1 + ((uint32_t)sh.cut_bin << shift1);
+      const unsigned long long nhi = (unsigned long long)nlo + ((1ull << shift1) - 1ull);
+      const uint32_t khi = nhi < (unsigned long long)key_max ? (uint32_t)nhi : key_max;
+      const unsigned long long above = sh.cut_above, at_mass = sh.cut_mass;
+      __syncthreads();
+      if (nlo == khi) {
+        r1 = SelResult{nlo, above + at_mass};
+      } else {
+        r1 = kind == 1 ? radix_select<TIn, false>(sh, cs, nlo, khi, target, -1.f, R, c, above)
+                       : radix_select<TIn, true>(sh, cs, nlo, khi, target, -1.f, R, c, above);
+      }
+    }
+    lo_key = r1.key;
+    kept_mass = r1.mass_ge;
+  }
+  if (k_on && p_on) {
+    const SelResult r2 = radix_select<TIn, true>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), R, c, 0ull);
+    lo_key = r2.key;
+    kept_mass = r2.mass_ge;
   }
   const float lo_val = K::value(lo_key);
 
   if (MODE == MODE_SAMPLE) {
     // ---- Gumbel-max over the kept set ------------------------------------
-    if (tid == 0) sh.best = 0ull;
-    __syncthreads();
-    gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, false, seed, a.step, (uint32_t)i);
+    gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, seed, a.step, (uint32_t)i);
     if (tid == 0) a.out_ids[i] = argmax_index(sh.best);
   } else {
     // ---- log-probs of the processed distribution -------------------------
@@ -837,11 +900,9 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     if (p_on) {
       lnS = logf(__ull2float_rn(kept_mass) / kMassScale);
     } else if (k_on) {
-      cs.each(lo_val, [&](float v, int64_t) {
-        atomicAdd(&sh.acc, __float2ull_rn(ex2(fmaf(v, c, -R)) * kMassScale));
-      });
+      cs.each(lo_val, [&](float v, int64_t) { add_mass(sh.acc, __float2ull_rn(ex2(fmaf(v, c, -R)) * kMassScale)); });
       __syncthreads();
-      lnS = logf(__ull2float_rn(sh.acc) / kMassScale);
+      lnS = logf(__ull2float_rn(read_mass(sh.acc)) / kMassScale);
     } else {
       lnS = logf(S);
     }
