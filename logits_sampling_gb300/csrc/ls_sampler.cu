@@ -58,6 +58,8 @@ struct KernelArgs {
   int32_t cand_cap;  // capacity of the shared-memory candidate list
 };
 
+constexpr int kGroupList = 2048;  // capacity of the candidate-group list
+
 // Fixed part of the dynamic shared memory; the group maxima follow it.
 struct Shared {
   // Histogram: u32 counts, or masses as (lo, hi) u32 pairs updated with
@@ -74,9 +76,12 @@ struct Shared {
   int cut_bin;
   int min_index;
   int cand_count;
+  int group_count;
+  int glist[kGroupList];  // candidate group indices (collection stage 1)
   float red_m[kWarps];
   float red_s[kWarps];
   float red_r[kWarps];
+  float row_M, row_S, row_gamma;
 };
 
 // Exact 64-bit add into a (lo, hi) pair of u32 counters with two native
@@ -90,6 +95,20 @@ __device__ __forceinline__ void add_mass(unsigned int* pair, unsigned long long 
 }
 __device__ __forceinline__ unsigned long long read_mass(const unsigned int* pair) {
   return ((unsigned long long)pair[1] << 32) | pair[0];
+}
+
+// round(w * 2^40) for a weight w in [0, 1], from the float's bits with integer
+// operations only (64-bit float/integer conversions run on the slow FP64
+// pipe).  Weights below 2^-41 give 0.
+__device__ __forceinline__ unsigned long long mass_fixed(float w) {
+  const uint32_t b = __float_as_uint(w);
+  const int e = (int)((b >> 23) & 0xFFu);
+  if (e == 0) return 0ull;
+  const unsigned long long mant = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 110;  // w * 2^40 = mant * 2^(e - 127 - 23 + 40)
+  if (sh >= 0) return mant << sh;
+  if (sh <= -25) return 0ull;
+  return (mant + (1ull << (-sh - 1))) >> (-sh);
 }
 
 // ---------------------------------------------------------------------------
@@ -451,7 +470,7 @@ __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo
       if (v <= hi && kk >= base && kk <= top) {
         const int bin = (int)((kk - base) >> shift);
         if (kMass)
-          add_mass(&sh.hist[2 * bin], __float2ull_rn(ex2(fmaf(v, c, -R)) * kMassScale));
+          add_mass(&sh.hist[2 * bin], mass_fixed(ex2(fmaf(v, c, -R))));
         else
           atomicAdd(&sh.hist[bin], 1u);
       }
@@ -576,18 +595,24 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // mass in the row (total, candidate and kept masses) uses this one formula,
   // so the rounding of R cancels in each ratio the cuts compare.  Each thread
   // keeps its own reference r = RN(m c) for its running maximum m.
+  // Two register stages: the loads of the next groups are in flight while
+  // the current ones are reduced.  Each thread also keeps its two largest
+  // group maxima and their slots (group = tid + slot * kThreads), which name
+  // its candidate groups later without a scan in the common case.
   using RV = RowView<TIn>;
   float m = kNegInf, r = 0.f;
   f32x2 acc = 0ull;
   const f32x2 c2 = pack2(c, c);
-  constexpr int U = RV::kBytes == 2 ? 4 : 2;
-  for (int g0 = tid; g0 < rv.NG; g0 += kThreads * U) {
-    uint32_t w[U][RV::kWords];
+  float top1 = kNegInf, top2 = kNegInf;
+  int slot1 = -1, slot2 = -1;
+  constexpr int U = RV::kBytes == 2 ? 2 : 1;  // groups per stage
+  constexpr int STEP = U * kThreads;
+  auto issue = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int g = g0 + u * kThreads;
-      if (rv.full(g)) rv.load_words(g, w[u]);
-    }
+    for (int u = 0; u < U; ++u)
+      if (rv.full(g0 + u * kThreads)) rv.load_words(g0 + u * kThreads, w[u]);
+  };
+  auto consume = [&](int g0, int slot0, uint32_t (&w)[U][RV::kWords]) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int g = g0 + u * kThreads;
@@ -595,6 +620,17 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
         if (!rv.full(g)) rv.load_words_partial(g, w[u]);
         const float gm = RV::group_max(w[u]);
         gmax[g] = gm;
+        if (gm > top2) {
+          if (gm > top1) {
+            top2 = top1;
+            slot2 = slot1;
+            top1 = gm;
+            slot1 = slot0 + u;
+          } else {
+            top2 = gm;
+            slot2 = slot0 + u;
+          }
+        }
         if (need_sum) {
           if (gm > m) {
             const float rn = __fmul_rn(gm, c);  // rounded: never fused into r - rn
@@ -608,6 +644,17 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
           m = fmaxf(m, gm);
         }
       }
+    }
+  };
+  {
+    uint32_t wa[U][RV::kWords], wb[U][RV::kWords];
+    issue(tid, wa);
+    int slot = 0;
+    for (int g0 = tid; g0 < rv.NG; g0 += 2 * STEP, slot += 2 * U) {
+      issue(g0 + STEP, wb);
+      consume(g0, slot, wa);
+      issue(g0 + 2 * STEP, wa);
+      consume(g0 + STEP, slot + U, wb);
     }
   }
   // ---- one block reduction: row maximum, total mass, top-k bound --------
@@ -660,27 +707,32 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     sh.acc[1] = 0u;
     sh.min_index = 0x7FFFFFFF;
     sh.cand_count = 0;
+    sh.group_count = 0;
   }
   __syncthreads();
-  float M = kNegInf, gamma = kPosInf;
-#pragma unroll
-  for (int q = 0; q < kWarps; ++q) {
-    M = fmaxf(M, sh.red_m[q]);
-    gamma = fminf(gamma, sh.red_f[q]);
+  // warp 0 combines the 16 warp results (fixed order, so S is deterministic)
+  if (tid < 32) {
+    const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
+    const float gq = lane < kWarps ? sh.red_f[lane] : kPosInf;
+    const float Mw = warp_reduce(mq, OpMax());
+    const float Gw = warp_reduce(gq, OpMin());
+    float sq = 0.f;
+    if (need_sum && Mw < kPosInf && mq > kNegInf) sq = sh.red_s[lane] * ex2(sh.red_r[lane] - __fmul_rn(Mw, c));
+    const float Sw = warp_reduce(sq, OpAddF());
+    if (lane == 0) {
+      sh.row_M = Mw;
+      sh.row_S = Sw;
+      sh.row_gamma = Gw;
+    }
   }
+  __syncthreads();
+  const float M = sh.row_M, gamma = sh.row_gamma;
   if (M == kNegInf) {
     row_error(a, i, MODE, LS_ROW_ERR_NO_FINITE);
     return;
   }
   const float R = __fmul_rn(M, c);  // reference exponent of the row (rounded product, never fused)
-  float S = 0.f;
-  if (need_sum && M < kPosInf) {
-#pragma unroll
-    for (int q = 0; q < kWarps; ++q) {
-      const float mq = sh.red_m[q];
-      if (mq > kNegInf) S += sh.red_s[q] * ex2(sh.red_r[q] - R);
-    }
-  }
+  float S = (need_sum && M < kPosInf) ? sh.row_S : 0.f;
   const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;
   const bool tie_only = greedy || M == kPosInf;  // no temperature-scaled distribution
 
@@ -737,42 +789,99 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // warp-aggregated atomic per warp and round) and feed the first select
   // level's histogram (4 sub-counters per bin against contention).
   using RVT = RowView<TIn>;
-  constexpr int GPR = RVT::kBytes == 2 ? 4 : 2;  // groups loaded per round
+  constexpr int GPR = 2;  // groups loaded per round
   int count = 0;
+  // Entry >= lc of a loaded group: append it to the list and feed the first
+  // select level's histogram.
+  auto take = [&](int g, const uint32_t (&w)[RVT::kWords], uint32_t mm, int at) {
+#pragma unroll 1
+    while (mm) {
+      const int e = __ffs(mm) - 1;
+      mm &= mm - 1u;
+      const float x = RVT::element(w, e);
+      if (at < a.cand_cap) {
+        cand_v[at] = x;
+        cand_j[at] = (int32_t)rv.index(g, e);
+      }
+      ++at;
+      if (kind != 0) {
+        const uint32_t kk = K::key(x);
+        if (kk >= klo1 && kk <= key_max) {
+          const int sub = (int)(((kk - klo1) >> shift1) << 2) | (lane & 3);
+          if (kind == 2)
+            add_mass(&sh.hist[2 * sub], mass_fixed(ex2(fmaf(x, c, -R))));
+          else
+            atomicAdd(&sh.hist[sub], 1u);
+        }
+      }
+    }
+  };
   if (lc <= M) {
     const int slots = (rv.NG + kThreads - 1) / kThreads;
-    for (int sbase = 0; sbase < slots; sbase += 32) {
-      uint32_t mask = 0u;
-      const int send = min(slots, sbase + 32);
-      for (int sl = sbase; sl < send; ++sl) {
-        const int g = tid + sl * kThreads;
-        if (g < rv.NG && gmax[g] >= lc) mask |= 1u << (sl - sbase);
+    // A thread whose second largest group maximum is below lc holds at most
+    // its top group as a candidate; otherwise it scans its slots.
+    const bool scan = top2 >= lc;
+    // ---- stage 1: candidate group indices -> shared list ----------------
+    constexpr int kChunks = 4;  // slots per thread <= 128 (vocab < 1M)
+    uint32_t cm[kChunks];
+#pragma unroll
+    for (int q = 0; q < kChunks; ++q) {
+      cm[q] = 0u;
+      if (scan) {
+        const int send = min(slots, 32 * q + 32);
+        for (int sl = 32 * q; sl < send; ++sl) {
+          const int g = tid + sl * kThreads;
+          if (g < rv.NG && gmax[g] >= lc) cm[q] |= 1u << (sl - 32 * q);
+        }
+      } else if (top1 >= lc && (slot1 >> 5) == q) {
+        cm[q] = 1u << (slot1 & 31);
       }
-      const int rounds = __reduce_max_sync(0xFFFFFFFFu, (__popc(mask) + GPR - 1) / GPR);
-      for (int rd = 0; rd < rounds; ++rd) {
-        uint32_t w[GPR][RVT::kWords];
-        int gg[GPR];
+    }
+    int gcnt = 0;
 #pragma unroll
-        for (int u = 0; u < GPR; ++u) {
-          gg[u] = -1;
-          if (mask) {
-            const int sl = __ffs(mask) - 1;
-            mask &= mask - 1u;
-            gg[u] = tid + (sbase + sl) * kThreads;
-            if (rv.full(gg[u])) rv.load_words(gg[u], w[u]);
-          }
-        }
-        uint32_t em[GPR];
-        int cnt = 0;
+    for (int q = 0; q < kChunks; ++q) gcnt += __popc(cm[q]);
+    {
+      int incl = gcnt;
 #pragma unroll
-        for (int u = 0; u < GPR; ++u) {
-          em[u] = 0u;
-          if (gg[u] >= 0) {
-            if (!rv.full(gg[u])) rv.load_words_partial(gg[u], w[u]);
-            em[u] = RVT::ge_mask(w[u], lc);
-            cnt += __popc(em[u]);
-          }
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t2;
+      }
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&sh.group_count, incl);
+      int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - gcnt;
+#pragma unroll
+      for (int q = 0; q < kChunks; ++q) {
+        uint32_t mm = cm[q];
+        while (mm) {
+          const int sl = 32 * q + __ffs(mm) - 1;
+          mm &= mm - 1u;
+          if (at < kGroupList) sh.glist[at] = tid + sl * kThreads;
+          ++at;
         }
+      }
+    }
+    __syncthreads();
+    const int ngroups = sh.group_count;
+    if (ngroups <= kGroupList) {
+      // ---- stage 2: two listed groups per thread per round -------------
+      for (int c0 = 0; c0 < ngroups; c0 += 2 * kThreads) {
+        const int ca = c0 + tid, cb = ca + kThreads;
+        const int ga = ca < ngroups ? sh.glist[ca] : -1;
+        const int gb = cb < ngroups ? sh.glist[cb] : -1;
+        uint32_t wa[RVT::kWords], wb[RVT::kWords];
+        if (ga >= 0 && rv.full(ga)) rv.load_words(ga, wa);
+        if (gb >= 0 && rv.full(gb)) rv.load_words(gb, wb);
+        uint32_t ma = 0u, mb = 0u;
+        if (ga >= 0) {
+          if (!rv.full(ga)) rv.load_words_partial(ga, wa);
+          ma = RVT::ge_mask(wa, lc);
+        }
+        if (gb >= 0) {
+          if (!rv.full(gb)) rv.load_words_partial(gb, wb);
+          mb = RVT::ge_mask(wb, lc);
+        }
+        const int cnt = __popc(ma) + __popc(mb);
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -781,30 +890,61 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
         }
         int base = 0;
         if (lane == 31) base = atomicAdd(&sh.cand_count, incl);
-        int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+        const int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+        if (ma) take(ga, wa, ma, at);
+        if (mb) take(gb, wb, mb, at + __popc(ma));
+      }
+    } else {
+      // ---- overflow: every thread collects its own candidate groups ------
+      for (int sbase = 0; sbase < slots; sbase += 32) {
+        uint32_t mask = 0u;
+        const int send = min(slots, sbase + 32);
+        if (scan) {
+          for (int sl = sbase; sl < send; ++sl) {
+            const int g = tid + sl * kThreads;
+            if (g < rv.NG && gmax[g] >= lc) mask |= 1u << (sl - sbase);
+          }
+        } else if (top1 >= lc && slot1 >= sbase && slot1 < send) {
+          mask = 1u << (slot1 - sbase);
+        }
+        const int rounds = __reduce_max_sync(0xFFFFFFFFu, (__popc(mask) + GPR - 1) / GPR);
+        for (int rd = 0; rd < rounds; ++rd) {
+          uint32_t w[GPR][RVT::kWords];
+          int gg[GPR];
 #pragma unroll
-        for (int u = 0; u < GPR; ++u) {
-          uint32_t mm = em[u];
-#pragma unroll 1
-          while (mm) {
-            const int e = __ffs(mm) - 1;
-            mm &= mm - 1u;
-            const float x = RVT::element(w[u], e);
-            if (at < a.cand_cap) {
-              cand_v[at] = x;
-              cand_j[at] = (int32_t)rv.index(gg[u], e);
+          for (int u = 0; u < GPR; ++u) {
+            gg[u] = -1;
+            if (mask) {
+              const int sl = __ffs(mask) - 1;
+              mask &= mask - 1u;
+              gg[u] = tid + (sbase + sl) * kThreads;
+              if (rv.full(gg[u])) rv.load_words(gg[u], w[u]);
             }
-            ++at;
-            if (kind != 0) {
-              const uint32_t kk = K::key(x);
-              if (kk >= klo1 && kk <= key_max) {
-                const int sub = (int)(((kk - klo1) >> shift1) << 2) | (lane & 3);
-                if (kind == 2)
-                  add_mass(&sh.hist[2 * sub], __float2ull_rn(ex2(fmaf(x, c, -R)) * kMassScale));
-                else
-                  atomicAdd(&sh.hist[sub], 1u);
-              }
+          }
+          uint32_t em[GPR];
+          int cnt = 0;
+#pragma unroll
+          for (int u = 0; u < GPR; ++u) {
+            em[u] = 0u;
+            if (gg[u] >= 0) {
+              if (!rv.full(gg[u])) rv.load_words_partial(gg[u], w[u]);
+              em[u] = RVT::ge_mask(w[u], lc);
+              cnt += __popc(em[u]);
             }
+          }
+          int incl = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t2;
+          }
+          int base = 0;
+          if (lane == 31) base = atomicAdd(&sh.cand_count, incl);
+          int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll
+          for (int u = 0; u < GPR; ++u) {
+            if (em[u]) take(gg[u], w[u], em[u], at);
+            at += __popc(em[u]);
           }
         }
       }
@@ -900,7 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     if (p_on) {
       lnS = logf(__ull2float_rn(kept_mass) / kMassScale);
     } else if (k_on) {
-      cs.each(lo_val, [&](float v, int64_t) { add_mass(sh.acc, __float2ull_rn(ex2(fmaf(v, c, -R)) * kMassScale)); });
+      cs.each(lo_val, [&](float v, int64_t) { add_mass(sh.acc, mass_fixed(ex2(fmaf(v, c, -R)))); });
       __syncthreads();
       lnS = logf(__ull2float_rn(read_mass(sh.acc)) / kMassScale);
     } else {
