@@ -378,22 +378,71 @@ struct Cands {
 // u >= exp(-exp(z - s_lb)).  That test (taken 1e-3 looser in g) runs on the
 // Philox word alone, and only entries passing it compute the two logarithms.
 // Leaves the winner's key in sh.best.
+// One Philox block yields the noise words of four consecutive vocabulary
+// entries; a thread walking consecutive entries reuses it.
+struct PhiloxCache {
+  uint32_t id = 0xFFFFFFFFu;
+  uint4 blk = make_uint4(0u, 0u, 0u, 0u);
+  __device__ __forceinline__ uint32_t word(uint64_t seed, uint64_t step, uint32_t row, int64_t j) {
+    const uint32_t b = (uint32_t)((uint64_t)j >> 2);
+    if (b != id) {
+      id = b;
+      blk = philox4x32_10(make_uint4(b, row, (uint32_t)step, (uint32_t)(step >> 32)),
+                          make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+    }
+    const uint32_t ln = (uint32_t)j & 3u;
+    return ln == 0 ? blk.x : ln == 1 ? blk.y : ln == 2 ? blk.z : blk.w;
+  }
+};
+
 template <typename TIn>
 __device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float lo, float T, uint64_t seed,
                               uint64_t step, uint32_t row) {
+  using RVT = RowView<TIn>;
   const float s_lb = f32_from_key((uint32_t)(sh.best >> 32));
   // z >= s_lb - 16.6356, in logit units (T > 0), lowered by a rounding margin
   float lb = (s_lb - 16.6366f) * T;
   lb -= fabsf(lb) * 1e-5f + 1e-30f;
-  cs.each(fmaxf(lo, lb), [&](float v, int64_t j) {
-    if (v >= M) return;
+  const float lo2 = fmaxf(lo, lb);
+  PhiloxCache pc;
+  auto test = [&](float v, int64_t j) {
     const float z = __fdiv_rn(v, T);
     const float need = s_lb - z - 1e-3f;
     const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
-    const uint32_t x = noise_word(seed, step, row, j);
+    const uint32_t x = pc.word(seed, step, row, j);
     const float u = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
     if (u >= thr) atomicMax(&sh.best, argmax_key(z + gumbel_of_word(x), j));
-  });
+  };
+  if (cs.listed) {
+    // each thread walks a contiguous run of the list (entries of one group are
+    // consecutive there), so neighbouring entries share Philox blocks
+    const int per = (cs.count + kThreads - 1) / kThreads;
+    const int c0 = threadIdx.x * per, c1 = min(cs.count, c0 + per);
+#pragma unroll 1
+    for (int q = c0; q < c1; ++q) {
+      const float v = cs.lv[q];
+      if (v >= lo2 && v < M) test(v, (int64_t)cs.lj[q]);
+    }
+  } else {
+    // candidate groups re-read from global memory, entries of a group in order
+    const RowView<TIn>& rv = *cs.rv;
+    for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
+      if (!(cs.gmax[g] >= lo2)) continue;
+      uint32_t w[RVT::kWords];
+      if (rv.full(g))
+        rv.load_words(g, w);
+      else
+        rv.load_words_partial(g, w);
+      uint32_t mm = RVT::ge_mask(w, lo2);
+#pragma unroll 1
+      while (mm) {
+        const int e = __ffs(mm) - 1;
+        mm &= mm - 1u;
+        const float v = RVT::element(w, e);
+        if (v < M) test(v, rv.index(g, e));
+      }
+    }
+  }
   __syncthreads();
 }
 
@@ -596,15 +645,11 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // so the rounding of R cancels in each ratio the cuts compare.  Each thread
   // keeps its own reference r = RN(m c) for its running maximum m.
   // Two register stages: the loads of the next groups are in flight while
-  // the current ones are reduced.  Each thread also keeps its two largest
-  // group maxima and their slots (group = tid + slot * kThreads), which name
-  // its candidate groups later without a scan in the common case.
+  // the current ones are reduced.
   using RV = RowView<TIn>;
   float m = kNegInf, r = 0.f;
   f32x2 acc = 0ull;
   const f32x2 c2 = pack2(c, c);
-  float top1 = kNegInf, top2 = kNegInf;
-  int slot1 = -1, slot2 = -1;
   constexpr int U = RV::kBytes == 2 ? 2 : 1;  // groups per stage
   constexpr int STEP = U * kThreads;
   auto issue = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
@@ -612,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     for (int u = 0; u < U; ++u)
       if (rv.full(g0 + u * kThreads)) rv.load_words(g0 + u * kThreads, w[u]);
   };
-  auto consume = [&](int g0, int slot0, uint32_t (&w)[U][RV::kWords]) {
+  auto consume = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int g = g0 + u * kThreads;
@@ -620,17 +665,6 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
         if (!rv.full(g)) rv.load_words_partial(g, w[u]);
         const float gm = RV::group_max(w[u]);
         gmax[g] = gm;
-        if (gm > top2) {
-          if (gm > top1) {
-            top2 = top1;
-            slot2 = slot1;
-            top1 = gm;
-            slot1 = slot0 + u;
-          } else {
-            top2 = gm;
-            slot2 = slot0 + u;
-          }
-        }
         if (need_sum) {
           if (gm > m) {
             const float rn = __fmul_rn(gm, c);  // rounded: never fused into r - rn
@@ -649,12 +683,11 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   {
     uint32_t wa[U][RV::kWords], wb[U][RV::kWords];
     issue(tid, wa);
-    int slot = 0;
-    for (int g0 = tid; g0 < rv.NG; g0 += 2 * STEP, slot += 2 * U) {
+    for (int g0 = tid; g0 < rv.NG; g0 += 2 * STEP) {
       issue(g0 + STEP, wb);
-      consume(g0, slot, wa);
+      consume(g0, wa);
       issue(g0 + 2 * STEP, wa);
-      consume(g0 + STEP, slot + U, wb);
+      consume(g0 + STEP, wb);
     }
   }
   // ---- one block reduction: row maximum, total mass, top-k bound --------
@@ -772,7 +805,10 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     lc = fminf(fmaxf(Lp, -FLT_MAX), M);
     kind = 2;
   } else {
-    lc = MODE == MODE_LOGPROBS ? kPosInf : lg;  // unfiltered log-probs need no candidates
+    // Unfiltered rows build no list: sampling reads only the groups above its
+    // noise bounds (the maximum's ties, then the pruned Gumbel pass) straight
+    // from global memory, and unfiltered log-probs need no candidates at all.
+    lc = kPosInf;
   }
   lc = fmaxf(lc, -FLT_MAX);
   const uint32_t key_max = K::key(M);
@@ -817,49 +853,28 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     }
   };
   if (lc <= M) {
-    const int slots = (rv.NG + kThreads - 1) / kThreads;
-    // A thread whose second largest group maximum is below lc holds at most
-    // its top group as a candidate; otherwise it scans its slots.
-    const bool scan = top2 >= lc;
     // ---- stage 1: candidate group indices -> shared list ----------------
-    constexpr int kChunks = 4;  // slots per thread <= 128 (vocab < 1M)
-    uint32_t cm[kChunks];
+    // Warp w sweeps groups [w * span, (w + 1) * span) of the shared-memory
+    // maxima, 32 at a time: a count pass, one prefix over the 16 warp counts,
+    // then a write pass.  Coalesced, branch-free, no atomics.
+    const int span = (rv.NG + kWarps - 1) / kWarps;
+    const int wbeg = (tid >> 5) * span, wend = min(rv.NG, wbeg + span);
+    int wcount = 0;
+    for (int g = wbeg + lane; g - lane < wend; g += 32)
+      wcount += __popc(__ballot_sync(0xFFFFFFFFu, g < wend && gmax[g] >= lc));
+    if (lane == 0) sh.red_i[tid >> 5] = wcount;
+    __syncthreads();
+    int wbase = 0;
 #pragma unroll
-    for (int q = 0; q < kChunks; ++q) {
-      cm[q] = 0u;
-      if (scan) {
-        const int send = min(slots, 32 * q + 32);
-        for (int sl = 32 * q; sl < send; ++sl) {
-          const int g = tid + sl * kThreads;
-          if (g < rv.NG && gmax[g] >= lc) cm[q] |= 1u << (sl - 32 * q);
-        }
-      } else if (top1 >= lc && (slot1 >> 5) == q) {
-        cm[q] = 1u << (slot1 & 31);
-      }
-    }
-    int gcnt = 0;
-#pragma unroll
-    for (int q = 0; q < kChunks; ++q) gcnt += __popc(cm[q]);
-    {
-      int incl = gcnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t2;
-      }
-      int base = 0;
-      if (lane == 31) base = atomicAdd(&sh.group_count, incl);
-      int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - gcnt;
-#pragma unroll
-      for (int q = 0; q < kChunks; ++q) {
-        uint32_t mm = cm[q];
-        while (mm) {
-          const int sl = 32 * q + __ffs(mm) - 1;
-          mm &= mm - 1u;
-          if (at < kGroupList) sh.glist[at] = tid + sl * kThreads;
-          ++at;
-        }
-      }
+    for (int q = 0; q < kWarps; ++q) wbase += q < (tid >> 5) ? sh.red_i[q] : 0;
+    if (tid == kThreads - 1) sh.group_count = wbase + wcount;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int g = wbeg + lane; g - lane < wend; g += 32) {
+      const bool hit = g < wend && gmax[g] >= lc;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, hit);
+      const int at = wbase + __popc(bal & lt);
+      if (hit && at < kGroupList) sh.glist[at] = g;
+      wbase += __popc(bal);
     }
     __syncthreads();
     const int ngroups = sh.group_count;
@@ -896,16 +911,13 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       }
     } else {
       // ---- overflow: every thread collects its own candidate groups ------
+      const int slots = (rv.NG + kThreads - 1) / kThreads;
       for (int sbase = 0; sbase < slots; sbase += 32) {
         uint32_t mask = 0u;
         const int send = min(slots, sbase + 32);
-        if (scan) {
-          for (int sl = sbase; sl < send; ++sl) {
-            const int g = tid + sl * kThreads;
-            if (g < rv.NG && gmax[g] >= lc) mask |= 1u << (sl - sbase);
-          }
-        } else if (top1 >= lc && slot1 >= sbase && slot1 < send) {
-          mask = 1u << (slot1 - sbase);
+        for (int sl = sbase; sl < send; ++sl) {
+          const int g = tid + sl * kThreads;
+          if (g < rv.NG && gmax[g] >= lc) mask |= 1u << (sl - sbase);
         }
         const int rounds = __reduce_max_sync(0xFFFFFFFFu, (__popc(mask) + GPR - 1) / GPR);
         for (int rd = 0; rd < rounds; ++rd) {
@@ -952,12 +964,12 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     __syncthreads();
     count = sh.cand_count;
   }
-  const Cands<TIn> cs{&rv, gmax, cand_v, cand_j, count, count <= a.cand_cap};
+  const Cands<TIn> cs{&rv, gmax, cand_v, cand_j, count, lc <= M && count <= a.cand_cap};
 
   // The maximum's ties: lowest index (greedy), count (log-probs of ties-only
   // rows) or exact Gumbel score (sampling; the best is a lower bound of the
   // winner's score).
-  if (lc <= M && (MODE == MODE_SAMPLE || tie_only)) {
+  if (MODE == MODE_SAMPLE || tie_only) {
     cs.each(M, [&](float x, int64_t j) {
       if (MODE == MODE_LOGPROBS) {
         atomicAdd(&sh.acc[0], 1u);
