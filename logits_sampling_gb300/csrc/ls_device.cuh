@@ -15,10 +15,6 @@ constexpr int kGroup = 16;               // logits per group: one 32-byte sector
 constexpr int kBinBits = 11;
 constexpr int kBins = 1 << kBinBits;     // bins per radix-select level
 constexpr int kBinsPerThread = kBins / kThreads;
-// The first select level is built while collecting candidates, with four
-// sub-counters per bin (lane mod 4) against atomic contention: 512 bins.
-constexpr int kBinBits1 = 9;
-static_assert((1 << kBinBits1) * 4 == kBins && (1 << kBinBits1) <= kThreads, "first-level bins");
 static_assert(kBins % kThreads == 0, "bins must split evenly over threads");
 
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -229,7 +225,8 @@ __device__ __forceinline__ unsigned long long block_exclusive_scan(unsigned long
   if (lane == 31) red[w] = incl;
   __syncthreads();
   unsigned long long base = 0;
-  for (int i = 0; i < w; ++i) base += red[i];
+#pragma unroll
+  for (int i = 0; i < kWarps - 1; ++i) base += i < w ? red[i] : 0ull;  // independent loads
   return base + incl - v;
 }
 

@@ -58,10 +58,16 @@ struct KernelArgs {
   int32_t cand_cap;  // capacity of the shared-memory candidate list
 };
 
-constexpr int kGroupList = 2048;  // capacity of the candidate-group list
+constexpr int kWarpList = 128;  // candidate groups a warp lists before loading them
+
+// Group-maximum slots of a row: worst-case row alignment, rounded up to whole
+// 16-byte vectors so that the maxima can be scanned four at a time.
+__host__ __device__ inline int64_t group_slots(int64_t vocab) {
+  return ((vocab + 2 * kGroup - 1) / kGroup + 3) & ~(int64_t)3;
+}
 
 // Fixed part of the dynamic shared memory; the group maxima follow it.
-struct Shared {
+struct alignas(16) Shared {
   // Histogram: u32 counts, or masses as (lo, hi) u32 pairs updated with
   // carry-propagating 32-bit atomics (shared-memory 64-bit adds are not
   // native and degrade badly under contention).
@@ -76,12 +82,9 @@ struct Shared {
   int cut_bin;
   int min_index;
   int cand_count;
-  int group_count;
-  int glist[kGroupList];  // candidate group indices (collection stage 1)
+  int glist[kWarps * kWarpList];  // candidate group indices, one slice per warp
   float red_m[kWarps];
   float red_s[kWarps];
-  float red_r[kWarps];
-  float row_M, row_S, row_gamma;
 };
 
 // Exact 64-bit add into a (lo, hi) pair of u32 counters with two native
@@ -395,6 +398,12 @@ struct PhiloxCache {
   }
 };
 
+// Exact Gumbel score of entry j (value x) raised into *best.
+__device__ __forceinline__ void score_entry(unsigned long long* best, float x, float T, uint64_t seed, uint64_t step,
+                                         uint32_t row, int64_t j) {
+  atomicMax(best, argmax_key(__fdiv_rn(x, T) + gumbel_of_word(noise_word(seed, step, row, j)), j));
+}
+
 template <typename TIn>
 __device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float lo, float T, uint64_t seed,
                               uint64_t step, uint32_t row) {
@@ -446,42 +455,77 @@ __device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float l
   __syncthreads();
 }
 
-// Find the highest bin b with above + sum_{b' >= b} hist[b'] >= target.  Writes
-// sh.cut_bin (-1 when the total never reaches target), sh.cut_above (weight
-// strictly above bin b, including `above`) and sh.cut_mass (hist[b]).
-template <bool kMass>
-__device__ __forceinline__ unsigned long long bin_weight(const Shared& sh, int b) {
-  return kMass ? read_mass(&sh.hist[2 * b]) : (unsigned long long)sh.hist[b];
-}
+// Bin weights of one select level.  A bin holds a count (top-k), the exact
+// fixed-point mass of its entries as a (lo, hi) pair (top-p, bins spanning
+// several keys) or, when every bin is a single key, a count that is scaled
+// here by that key's weight: the same fixed-point mass, since every entry of
+// the bin has the same value.
+enum BinMode { BIN_COUNT = 0, BIN_MASS = 1, BIN_KEY_COUNT = 2 };
 
-template <bool kMass>
-__device__ __forceinline__ void find_cut_bin(Shared& sh, int nb, unsigned long long above, unsigned long long target) {
-  const int t = threadIdx.x;
+template <typename TIn>
+struct BinWeight {
+  const Shared* sh;
+  int mode;
+  uint32_t klo;  // key of bin 0 (BIN_KEY_COUNT)
+  float c, R;
+  __device__ __forceinline__ unsigned long long operator()(int b) const {
+    if (mode == BIN_MASS) return read_mass(&sh->hist[2 * b]);
+    const unsigned int n = sh->hist[b];
+    if (mode == BIN_COUNT || n == 0u) return n;
+    return (unsigned long long)n * mass_fixed(ex2(fmaf(KeyOps<TIn>::value(klo + (uint32_t)b), c, -R)));
+  }
+};
+
+// Find the highest bin b with above + (weight of bins >= b) >= target.
+// Thread t holds bins nb-1-4t .. nb-4-4t; one block scan over the threads.
+// With joint_p >= 0 the target becomes joint_p * (total weight of the level)
+// (written back to `target`, the same in every thread).
+// Writes sh.cut_bin (-1 when the total never reaches the target, possible
+// only through rounding of a top-p target), sh.cut_above (weight strictly
+// above bin b, including `above`) and sh.cut_mass (weight of bin b); returns
+// the level's total weight.  Two block barriers.
+template <typename W>
+__device__ __forceinline__ unsigned long long find_cut_bin(Shared& sh, int nb, unsigned long long above,
+                                                           unsigned long long& target, float joint_p,
+                                                           const W& weight) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int top = nb - 1 - t * kBinsPerThread;
   unsigned long long local = 0;
 #pragma unroll
-  for (int q = 0; q < kBinsPerThread; ++q) {
-    const int b = top - q;
-    if (b >= 0) local += bin_weight<kMass>(sh, b);
+  for (int q = 0; q < kBinsPerThread; ++q) local += top - q >= 0 ? weight(top - q) : 0ull;
+  unsigned long long incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
   }
   if (t == 0) sh.cut_bin = -1;
-  unsigned long long cum = above + block_exclusive_scan(local, sh.red_u64);
-  if (cum < target && cum + local >= target) {
+  if (lane == 31) sh.red_u64[warp] = incl;
+  __syncthreads();
+  unsigned long long base = 0, total = 0;
 #pragma unroll
-    for (int q = 0; q < kBinsPerThread; ++q) {
-      const int b = top - q;
-      if (b < 0) break;
-      const unsigned long long h = bin_weight<kMass>(sh, b);
-      if (cum + h >= target) {
-        sh.cut_bin = b;
+  for (int i = 0; i < kWarps; ++i) {
+    const unsigned long long x = sh.red_u64[i];
+    base += i < warp ? x : 0ull;
+    total += x;
+  }
+  if (joint_p >= 0.f) target = __float2ull_ru(joint_p * __ull2float_rn(total));
+  if (target < 1ull) target = 1ull;
+  unsigned long long cum = above + base + incl - local;
+  if (cum < target && cum + local >= target) {
+    for (int q = 0; q < kBinsPerThread; ++q) {  // one thread: weights taken again
+      const unsigned long long wq = weight(top - q);
+      if (cum + wq >= target) {
+        sh.cut_bin = top - q;
         sh.cut_above = cum;
-        sh.cut_mass = h;
+        sh.cut_mass = wq;
         break;
       }
-      cum += h;
+      cum += wq;
     }
   }
   __syncthreads();
+  return total;
 }
 
 struct SelResult {
@@ -491,64 +535,59 @@ struct SelResult {
 
 // Exact threshold select over the row entries with keys in [klo, khi], given
 // the weight `above` of the entries with larger keys: returns the largest key
-// kappa such that above + (weight of entries with key in [kappa, khi]) >= target, where weight is 1 (top-k, target = k) or the
-// fixed-point probability mass exp((l - M)/T) * 2^40 (top-p).  With
-// joint_p >= 0 the target is joint_p * (total weight of the range), taken from
-// the first level's histogram.  Each level splits the remaining key range into
-// at most 2048 bins: bf16 keys (16 bits) need at most two levels, fp32 keys at
-// most three.  If the total weight never reaches the target (possible only
-// through rounding of a top-p target) the whole range is kept.
-template <typename TIn, bool kMass>
+// kappa such that above + (weight of entries with key in [kappa, khi]) >=
+// target, where weight is 1 (top-k, target = k) or the fixed-point
+// probability mass exp((l - M)/T) * 2^40 (top-p, `mass`).  With joint_p >= 0
+// the target is joint_p * (total weight of the range).  Each level splits the
+// remaining key range into at most 2048 bins: bf16 keys (16 bits) need at most
+// two levels, fp32 keys at most three.  With `built` the first level's
+// histogram (same binning) is already in shared memory.  If the total weight
+// never reaches the target (possible only through rounding of a top-p target)
+// the whole range is kept.
+template <typename TIn>
 __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo, uint32_t khi,
                                   unsigned long long target, float joint_p, float R, float c,
-                                  unsigned long long above) {
+                                  unsigned long long above, bool mass, bool built) {
   using K = KeyOps<TIn>;
   unsigned long long mass_at = 0;
-  bool first = true;
-  do {
+  for (;;) {
     const uint32_t width = khi - klo;
     const int bits = width ? 32 - __clz(width) : 0;
     const int shift = bits > kBinBits ? bits - kBinBits : 0;
     const int nb = (int)(width >> shift) + 1;
-    for (int b = threadIdx.x; b < (kMass ? 2 * nb : nb); b += kThreads) sh.hist[b] = 0u;
-    __syncthreads();
-    const float lo = K::value(klo), hi = K::value(khi);
-    const uint32_t base = klo, top = khi;
-    cs.each(lo, [&](float v, int64_t) {
-      const uint32_t kk = K::key(v);
-      if (v <= hi && kk >= base && kk <= top) {
-        const int bin = (int)((kk - base) >> shift);
-        if (kMass)
-          add_mass(&sh.hist[2 * bin], mass_fixed(ex2(fmaf(v, c, -R))));
-        else
-          atomicAdd(&sh.hist[bin], 1u);
-      }
-    });
-    __syncthreads();
-    if (first && joint_p >= 0.f) {
-      unsigned long long part = 0;
-      for (int b = threadIdx.x; b < nb; b += kThreads) part += bin_weight<kMass>(sh, b);
-      const unsigned long long total = block_reduce(part, OpAddU64(), sh.red_u64);
-      target = __float2ull_ru(joint_p * __ull2float_rn(total));
+    const int mode = !mass ? BIN_COUNT : shift == 0 ? BIN_KEY_COUNT : BIN_MASS;
+    if (!built) {
+      for (int b = threadIdx.x; b < (mode == BIN_MASS ? 2 * nb : nb); b += kThreads) sh.hist[b] = 0u;
+      __syncthreads();
+      const float lo = K::value(klo), hi = K::value(khi);
+      const uint32_t base = klo, top = khi;
+      cs.each(lo, [&](float v, int64_t) {
+        const uint32_t kk = K::key(v);
+        if (v <= hi && kk >= base && kk <= top) {
+          const int bin = (int)((kk - base) >> shift);
+          if (mode == BIN_MASS)
+            add_mass(&sh.hist[2 * bin], mass_fixed(ex2(fmaf(v, c, -R))));
+          else
+            atomicAdd(&sh.hist[bin], 1u);
+        }
+      });
+      __syncthreads();
     }
-    if (target < 1ull) target = 1ull;
-    find_cut_bin<kMass>(sh, nb, above, target);
+    built = false;
+    const unsigned long long total =
+        find_cut_bin(sh, nb, above, target, joint_p, BinWeight<TIn>{&sh, mode, klo, c, R});
+    joint_p = -1.f;
     const int b = sh.cut_bin;
-    if (b < 0) {  // only reachable on the first level
-      unsigned long long part = 0;
-      for (int q = threadIdx.x; q < nb; q += kThreads) part += bin_weight<kMass>(sh, q);
-      const unsigned long long total = block_reduce(part, OpAddU64(), sh.red_u64);
-      return SelResult{klo, above + total};
-    }
+    if (b < 0) return SelResult{klo, above + total};  // only reachable on the first level
     above = sh.cut_above;
     mass_at = sh.cut_mass;
     const uint32_t nlo = klo + ((uint32_t)b << shift);
     const unsigned long long nhi = (unsigned long long)nlo + ((1ull << shift) - 1ull);
     khi = nhi < (unsigned long long)khi ? (uint32_t)nhi : khi;
     klo = nlo;
-    first = false;
-    __syncthreads();
-  } while (klo < khi);
+    if (klo >= khi) break;  // a single key left
+    __syncthreads();        // the cut fields and the histogram are rewritten by the next level
+  }
   return SelResult{klo, above + mass_at};
 }
 
@@ -601,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   float* gmax = reinterpret_cast<float*>(smem_raw + sizeof(Shared));
   const int tid = threadIdx.x;
-  const int64_t ng_cap = (a.vocab + 2 * kGroup - 1) / kGroup;  // group maxima: worst-case row alignment
+  const int64_t ng_cap = group_slots(a.vocab);
   float* cand_v = gmax + ng_cap;
   int32_t* cand_j = reinterpret_cast<int32_t*>(cand_v + a.cand_cap);
   const int64_t i = blockIdx.x;
@@ -626,16 +665,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     return;
   }
 
-  const float T = a.temperature[req];
-  const int32_t k = a.top_k[req];
-  const float p = a.top_p[req];
   const int64_t V = a.vocab;
-  const bool greedy = !(T >= 1e-5f);
-  const bool k_on = !greedy && (ROUTE & ROUTE_K) && k >= 1 && (int64_t)k < V;
-  const bool p_on = !greedy && (ROUTE & ROUTE_P) && p < 0.99999f;
-  const bool need_sum = !greedy && !k_on && (p_on || MODE == MODE_LOGPROBS);
-  const float c = greedy ? 0.f : kLog2e / T;
-
   RowView<TIn> rv;
   rv.init(a.logits, src, a.stride, V);
 
@@ -645,11 +675,9 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // so the rounding of R cancels in each ratio the cuts compare.  Each thread
   // keeps its own reference r = RN(m c) for its running maximum m.
   // Two register stages: the loads of the next groups are in flight while
-  // the current ones are reduced.
+  // the current ones are reduced.  The first two stages are issued before
+  // the request's parameters are read.
   using RV = RowView<TIn>;
-  float m = kNegInf, r = 0.f;
-  f32x2 acc = 0ull;
-  const f32x2 c2 = pack2(c, c);
   constexpr int U = RV::kBytes == 2 ? 2 : 1;  // groups per stage
   constexpr int STEP = U * kThreads;
   auto issue = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
@@ -657,6 +685,22 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     for (int u = 0; u < U; ++u)
       if (rv.full(g0 + u * kThreads)) rv.load_words(g0 + u * kThreads, w[u]);
   };
+  uint32_t wa[U][RV::kWords], wb[U][RV::kWords];
+  issue(tid, wa);
+  issue(tid + STEP, wb);
+
+  const float T = a.temperature[req];
+  const int32_t k = a.top_k[req];
+  const float p = a.top_p[req];
+  const bool greedy = !(T >= 1e-5f);
+  const bool k_on = !greedy && (ROUTE & ROUTE_K) && k >= 1 && (int64_t)k < V;
+  const bool p_on = !greedy && (ROUTE & ROUTE_P) && p < 0.99999f;
+  const bool need_sum = !greedy && !k_on && (p_on || MODE == MODE_LOGPROBS);
+  const float c = greedy ? 0.f : kLog2e / T;
+
+  float m = kNegInf, r = 0.f;
+  f32x2 acc = 0ull;
+  const f32x2 c2 = pack2(c, c);
   auto consume = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -680,42 +724,33 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       }
     }
   };
-  {
-    uint32_t wa[U][RV::kWords], wb[U][RV::kWords];
-    issue(tid, wa);
-    for (int g0 = tid; g0 < rv.NG; g0 += 2 * STEP) {
-      issue(g0 + STEP, wb);
-      consume(g0, wa);
-      issue(g0 + 2 * STEP, wa);
-      consume(g0 + STEP, wb);
-    }
+  for (int g0 = tid; g0 < rv.NG; g0 += 2 * STEP) {
+    consume(g0, wa);
+    issue(g0 + 2 * STEP, wa);
+    consume(g0 + STEP, wb);
+    issue(g0 + 3 * STEP, wb);
   }
   // ---- one block reduction: row maximum, total mass, top-k bound --------
-  // (max, sum relative to RN(max * c)) pairs combine like an online softmax.
-  // For a top-k row each warp also extracts the j-th largest of its 32 thread
-  // maxima, j = ceil(k / 16): all 16 warps then hold >= j thread maxima (hence
-  // >= k distinct entries) at or above the smallest of those, gamma.
-  for (int q = tid; q < 2 * kBins; q += kThreads) sh.hist[q] = 0u;  // first-level histogram
+  // Each warp reduces its maximum, rescales every lane's sum to the warp's
+  // reference RN(max * c) and adds; after one barrier every warp combines the
+  // 16 warp results the same way (fixed order, so S is deterministic and the
+  // same in every warp).  For a top-k row each warp also extracts the j-th
+  // largest of its 32 thread maxima, j = ceil(k / 16): all 16 warps then hold
+  // >= j thread maxima (hence >= k distinct entries) at or above the smallest
+  // of those, gamma.
+  {
+    uint4* h4 = reinterpret_cast<uint4*>(sh.hist);
+    for (int q = tid; q < 2 * kBins / 4; q += kThreads) h4[q] = make_uint4(0u, 0u, 0u, 0u);
+  }
   const int lane = tid & 31;
   {
-    float mw = m, sw = 0.f, rw = r;
-    if (need_sum) {
+    const float mw = warp_reduce(m, OpMax());
+    float sw = 0.f;
+    if (need_sum && mw > kNegInf) {
       float lo, hi;
       unpack2(acc, lo, hi);
-      sw = lo + hi;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, mw, o);
-      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, sw, o);
-      const float r2 = __shfl_xor_sync(0xFFFFFFFFu, rw, o);
-      const float mx = fmaxf(mw, m2);
-      if (need_sum && mx > kNegInf) {
-        const float rx = __fmul_rn(mx, c);
-        sw = (mw > kNegInf ? sw * ex2(rw - rx) : 0.f) + (m2 > kNegInf ? s2 * ex2(r2 - rx) : 0.f);
-        rw = rx;
-      }
-      mw = mx;
+      sw = m > kNegInf ? (lo + hi) * ex2(r - __fmul_rn(mw, c)) : 0.f;
+      sw = warp_reduce(sw, OpAddF());
     }
     float gj = kNegInf;
     if (k_on && k <= 32 * kWarps) {
@@ -730,7 +765,6 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     if (lane == 0) {
       sh.red_m[tid >> 5] = mw;
       sh.red_s[tid >> 5] = sw;
-      sh.red_r[tid >> 5] = rw;
       sh.red_f[tid >> 5] = gj;
     }
   }
@@ -740,32 +774,21 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     sh.acc[1] = 0u;
     sh.min_index = 0x7FFFFFFF;
     sh.cand_count = 0;
-    sh.group_count = 0;
   }
   __syncthreads();
-  // warp 0 combines the 16 warp results (fixed order, so S is deterministic)
-  if (tid < 32) {
-    const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
-    const float gq = lane < kWarps ? sh.red_f[lane] : kPosInf;
-    const float Mw = warp_reduce(mq, OpMax());
-    const float Gw = warp_reduce(gq, OpMin());
-    float sq = 0.f;
-    if (need_sum && Mw < kPosInf && mq > kNegInf) sq = sh.red_s[lane] * ex2(sh.red_r[lane] - __fmul_rn(Mw, c));
-    const float Sw = warp_reduce(sq, OpAddF());
-    if (lane == 0) {
-      sh.row_M = Mw;
-      sh.row_S = Sw;
-      sh.row_gamma = Gw;
-    }
-  }
-  __syncthreads();
-  const float M = sh.row_M, gamma = sh.row_gamma;
+  const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
+  const float M = warp_reduce(mq, OpMax());
+  const float gamma = warp_reduce(lane < kWarps ? sh.red_f[lane] : kPosInf, OpMin());
   if (M == kNegInf) {
     row_error(a, i, MODE, LS_ROW_ERR_NO_FINITE);
     return;
   }
   const float R = __fmul_rn(M, c);  // reference exponent of the row (rounded product, never fused)
-  float S = (need_sum && M < kPosInf) ? sh.row_S : 0.f;
+  float S = 0.f;
+  if (need_sum && M < kPosInf) {
+    const float sq = lane < kWarps && mq > kNegInf ? sh.red_s[lane] * ex2(__fmul_rn(mq, c) - R) : 0.f;
+    S = warp_reduce(sq, OpAddF());
+  }
   const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;
   const bool tie_only = greedy || M == kPosInf;  // no temperature-scaled distribution
 
@@ -815,17 +838,24 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   const uint32_t klo1 = K::key(lc);
   const uint32_t width1 = key_max - klo1;
   const int bits1 = width1 ? 32 - __clz(width1) : 0;
-  const int shift1 = bits1 > kBinBits1 ? bits1 - kBinBits1 : 0;
-  const int nb1 = (int)(width1 >> shift1) + 1;
+  const int shift1 = bits1 > kBinBits ? bits1 - kBinBits : 0;
+  // first select level, built while collecting (the binning radix_select uses)
+  const int mode1 = kind == 1 ? BIN_COUNT : shift1 == 0 ? BIN_KEY_COUNT : BIN_MASS;
+  // sampling rows score the maximum's ties while collecting
+  const bool ties_in_take = MODE == MODE_SAMPLE && !tie_only;
 
-  // ---- collect: each thread loads its own candidate groups --------------
-  // A thread wrote the maxima of groups tid, tid + 512, ...; the candidate
-  // ones (maximum >= lc) are loaded a few at a time with all loads in flight
-  // at once.  Their entries >= lc are appended to the shared-memory list (one
-  // warp-aggregated atomic per warp and round) and feed the first select
-  // level's histogram (4 sub-counters per bin against contention).
+  // ---- collect: candidate groups -> entries >= lc -----------------------
+  // Each warp scans chunks of 128 group maxima (four per lane, one 16-byte
+  // shared load), chunk q going to warp q mod 16, and lists its candidate
+  // groups (maximum >= lc) in its own slice of the group list.  When the
+  // slice could overflow, and at the end, the warp loads the listed groups
+  // (two per lane per round, all loads in flight at once) and takes their
+  // entries >= lc: they are appended to the shared-memory candidate list (one
+  // atomic per warp and round), feed the first select level's histogram and,
+  // when sampling, the maximum's ties get their exact Gumbel score (the best
+  // is a lower bound of the winner's score).  No block barrier until every
+  // warp is done.
   using RVT = RowView<TIn>;
-  constexpr int GPR = 2;  // groups loaded per round
   int count = 0;
   // Entry >= lc of a loaded group: append it to the list and feed the first
   // select level's histogram.
@@ -843,60 +873,43 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       if (kind != 0) {
         const uint32_t kk = K::key(x);
         if (kk >= klo1 && kk <= key_max) {
-          const int sub = (int)(((kk - klo1) >> shift1) << 2) | (lane & 3);
-          if (kind == 2)
-            add_mass(&sh.hist[2 * sub], mass_fixed(ex2(fmaf(x, c, -R))));
+          const int bin = (int)((kk - klo1) >> shift1);
+          if (mode1 == BIN_MASS)
+            add_mass(&sh.hist[2 * bin], mass_fixed(ex2(fmaf(x, c, -R))));
           else
-            atomicAdd(&sh.hist[sub], 1u);
+            atomicAdd(&sh.hist[bin], 1u);
         }
       }
+      if (ties_in_take && x >= M) score_entry(&sh.best, x, T, seed, a.step, (uint32_t)i, rv.index(g, e));
     }
   };
   if (lc <= M) {
-    // ---- stage 1: candidate group indices -> shared list ----------------
-    // Warp w sweeps groups [w * span, (w + 1) * span) of the shared-memory
-    // maxima, 32 at a time: a count pass, one prefix over the 16 warp counts,
-    // then a write pass.  Coalesced, branch-free, no atomics.
-    const int span = (rv.NG + kWarps - 1) / kWarps;
-    const int wbeg = (tid >> 5) * span, wend = min(rv.NG, wbeg + span);
-    int wcount = 0;
-    for (int g = wbeg + lane; g - lane < wend; g += 32)
-      wcount += __popc(__ballot_sync(0xFFFFFFFFu, g < wend && gmax[g] >= lc));
-    if (lane == 0) sh.red_i[tid >> 5] = wcount;
-    __syncthreads();
-    int wbase = 0;
+    int* wl = sh.glist + (tid >> 5) * kWarpList;
+    // load the n listed groups of this warp (kPer per lane per round, all
+    // loads in flight at once) and take their entries
+    constexpr int kPer = RVT::kWords <= 8 ? 2 : 1;
+    auto flush = [&](int n) {
+      __syncwarp();
+      for (int c0 = 0; c0 < n; c0 += 32 * kPer) {
+        uint32_t w[kPer][RVT::kWords];
+        int gg[kPer];
 #pragma unroll
-    for (int q = 0; q < kWarps; ++q) wbase += q < (tid >> 5) ? sh.red_i[q] : 0;
-    if (tid == kThreads - 1) sh.group_count = wbase + wcount;
-    const unsigned lt = (1u << lane) - 1u;
-    for (int g = wbeg + lane; g - lane < wend; g += 32) {
-      const bool hit = g < wend && gmax[g] >= lc;
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, hit);
-      const int at = wbase + __popc(bal & lt);
-      if (hit && at < kGroupList) sh.glist[at] = g;
-      wbase += __popc(bal);
-    }
-    __syncthreads();
-    const int ngroups = sh.group_count;
-    if (ngroups <= kGroupList) {
-      // ---- stage 2: two listed groups per thread per round -------------
-      for (int c0 = 0; c0 < ngroups; c0 += 2 * kThreads) {
-        const int ca = c0 + tid, cb = ca + kThreads;
-        const int ga = ca < ngroups ? sh.glist[ca] : -1;
-        const int gb = cb < ngroups ? sh.glist[cb] : -1;
-        uint32_t wa[RVT::kWords], wb[RVT::kWords];
-        if (ga >= 0 && rv.full(ga)) rv.load_words(ga, wa);
-        if (gb >= 0 && rv.full(gb)) rv.load_words(gb, wb);
-        uint32_t ma = 0u, mb = 0u;
-        if (ga >= 0) {
-          if (!rv.full(ga)) rv.load_words_partial(ga, wa);
-          ma = RVT::ge_mask(wa, lc);
+        for (int u = 0; u < kPer; ++u) {
+          const int cu = c0 + 32 * u + lane;
+          gg[u] = cu < n ? wl[cu] : -1;
+          if (gg[u] >= 0 && rv.full(gg[u])) rv.load_words(gg[u], w[u]);
         }
-        if (gb >= 0) {
-          if (!rv.full(gb)) rv.load_words_partial(gb, wb);
-          mb = RVT::ge_mask(wb, lc);
+        uint32_t mm[kPer];
+        int cnt = 0;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          mm[u] = 0u;
+          if (gg[u] >= 0) {
+            if (!rv.full(gg[u])) rv.load_words_partial(gg[u], w[u]);
+            mm[u] = RVT::ge_mask(w[u], lc);
+            cnt += __popc(mm[u]);
+          }
         }
-        const int cnt = __popc(ma) + __popc(mb);
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -905,71 +918,50 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
         }
         int base = 0;
         if (lane == 31) base = atomicAdd(&sh.cand_count, incl);
-        const int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
-        if (ma) take(ga, wa, ma, at);
-        if (mb) take(gb, wb, mb, at + __popc(ma));
-      }
-    } else {
-      // ---- overflow: every thread collects its own candidate groups ------
-      const int slots = (rv.NG + kThreads - 1) / kThreads;
-      for (int sbase = 0; sbase < slots; sbase += 32) {
-        uint32_t mask = 0u;
-        const int send = min(slots, sbase + 32);
-        for (int sl = sbase; sl < send; ++sl) {
-          const int g = tid + sl * kThreads;
-          if (g < rv.NG && gmax[g] >= lc) mask |= 1u << (sl - sbase);
-        }
-        const int rounds = __reduce_max_sync(0xFFFFFFFFu, (__popc(mask) + GPR - 1) / GPR);
-        for (int rd = 0; rd < rounds; ++rd) {
-          uint32_t w[GPR][RVT::kWords];
-          int gg[GPR];
+        int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
 #pragma unroll
-          for (int u = 0; u < GPR; ++u) {
-            gg[u] = -1;
-            if (mask) {
-              const int sl = __ffs(mask) - 1;
-              mask &= mask - 1u;
-              gg[u] = tid + (sbase + sl) * kThreads;
-              if (rv.full(gg[u])) rv.load_words(gg[u], w[u]);
-            }
-          }
-          uint32_t em[GPR];
-          int cnt = 0;
-#pragma unroll
-          for (int u = 0; u < GPR; ++u) {
-            em[u] = 0u;
-            if (gg[u] >= 0) {
-              if (!rv.full(gg[u])) rv.load_words_partial(gg[u], w[u]);
-              em[u] = RVT::ge_mask(w[u], lc);
-              cnt += __popc(em[u]);
-            }
-          }
-          int incl = cnt;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += t2;
-          }
-          int base = 0;
-          if (lane == 31) base = atomicAdd(&sh.cand_count, incl);
-          int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
-#pragma unroll
-          for (int u = 0; u < GPR; ++u) {
-            if (em[u]) take(gg[u], w[u], em[u], at);
-            at += __popc(em[u]);
-          }
+        for (int u = 0; u < kPer; ++u) {
+          if (mm[u]) take(gg[u], w[u], mm[u], at);
+          at += __popc(mm[u]);
         }
       }
+      __syncwarp();
+    };
+    const unsigned lt = (1u << lane) - 1u;
+    const int nchunk = (rv.NG + 127) >> 7;
+    int wn = 0;
+    for (int q = tid >> 5; q < nchunk; q += kWarps) {
+      const int g0 = (q << 7) + 4 * lane;
+      float4 m4 = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+      if (g0 < rv.NG) m4 = *reinterpret_cast<const float4*>(gmax + g0);
+      const bool h0 = m4.x >= lc;
+      const bool h1 = g0 + 1 < rv.NG && m4.y >= lc;
+      const bool h2 = g0 + 2 < rv.NG && m4.z >= lc;
+      const bool h3 = g0 + 3 < rv.NG && m4.w >= lc;
+      const unsigned b0 = __ballot_sync(0xFFFFFFFFu, h0), b1 = __ballot_sync(0xFFFFFFFFu, h1);
+      const unsigned b2 = __ballot_sync(0xFFFFFFFFu, h2), b3 = __ballot_sync(0xFFFFFFFFu, h3);
+      const int tot = __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+      if (__builtin_expect(wn + tot > kWarpList, 0)) {
+        flush(wn);
+        wn = 0;
+      }
+      int pos = wn + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
+      if (h0) wl[pos++] = g0;
+      if (h1) wl[pos++] = g0 + 1;
+      if (h2) wl[pos++] = g0 + 2;
+      if (h3) wl[pos] = g0 + 3;
+      wn += tot;
     }
+    flush(wn);
     __syncthreads();
     count = sh.cand_count;
   }
   const Cands<TIn> cs{&rv, gmax, cand_v, cand_j, count, lc <= M && count <= a.cand_cap};
 
-  // The maximum's ties: lowest index (greedy), count (log-probs of ties-only
-  // rows) or exact Gumbel score (sampling; the best is a lower bound of the
-  // winner's score).
-  if (MODE == MODE_SAMPLE || tie_only) {
+  // The maximum's ties, unless collecting already scored them: lowest index
+  // (greedy), count (log-probs of ties-only rows) or exact Gumbel score
+  // (sampling; the best is a lower bound of the winner's score).
+  if (tie_only || (MODE == MODE_SAMPLE && !(lc <= M))) {
     cs.each(M, [&](float x, int64_t j) {
       if (MODE == MODE_LOGPROBS) {
         atomicAdd(&sh.acc[0], 1u);
@@ -996,47 +988,16 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   uint32_t lo_key = K::key(-FLT_MAX);  // no filter: every finite entry
   unsigned long long kept_mass = 0ull;
   if (kind != 0) {
-    // first level from the histogram built while collecting: one bin per
-    // thread, scanned from the highest bin down
+    // the first level's histogram was built while collecting
     const unsigned long long target =
         kind == 1 ? (unsigned long long)k : max(1ull, __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale));
-    unsigned long long h = 0ull;
-    const int b = nb1 - 1 - tid;
-    if (b >= 0) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        h += kind == 2 ? read_mass(&sh.hist[2 * (4 * b + q)]) : (unsigned long long)sh.hist[4 * b + q];
-    }
-    if (tid == 0) sh.cut_bin = -1;
-    const unsigned long long cum = block_exclusive_scan(h, sh.red_u64);
-    if (b >= 0 && cum < target && cum + h >= target) {
-      sh.cut_bin = b;
-      sh.cut_above = cum;
-      sh.cut_mass = h;
-    }
-    __syncthreads();
-    SelResult r1;
-    if (sh.cut_bin < 0) {  // only through rounding of a top-p target: keep every candidate
-      const unsigned long long part = b >= 0 ? h : 0ull;
-      r1 = SelResult{klo1, block_reduce(part, OpAddU64(), sh.red_u64)};
-    } else {
-      const uint32_t nlo = klo1 + ((uint32_t)sh.cut_bin << shift1);
-      const unsigned long long nhi = (unsigned long long)nlo + ((1ull << shift1) - 1ull);
-      const uint32_t khi = nhi < (unsigned long long)key_max ? (uint32_t)nhi : key_max;
-      const unsigned long long above = sh.cut_above, at_mass = sh.cut_mass;
-      __syncthreads();
-      if (nlo == khi) {
-        r1 = SelResult{nlo, above + at_mass};
-      } else {
-        r1 = kind == 1 ? radix_select<TIn, false>(sh, cs, nlo, khi, target, -1.f, R, c, above)
-                       : radix_select<TIn, true>(sh, cs, nlo, khi, target, -1.f, R, c, above);
-      }
-    }
+    const SelResult r1 = radix_select<TIn>(sh, cs, klo1, key_max, target, -1.f, R, c, 0ull, kind == 2, true);
     lo_key = r1.key;
     kept_mass = r1.mass_ge;
   }
   if (k_on && p_on) {
-    const SelResult r2 = radix_select<TIn, true>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), R, c, 0ull);
+    const SelResult r2 =
+        radix_select<TIn>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), R, c, 0ull, true, false);
     lo_key = r2.key;
     kept_mass = r2.mass_ge;
   }
@@ -1072,17 +1033,20 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
 // Shared memory of one CTA: fixed part, group maxima (worst-case row
 // alignment), candidate list of `cap` (value, index) pairs.
 static size_t smem_bytes(int64_t vocab, int cap) {
-  const int64_t ng = (vocab + 2 * kGroup - 1) / kGroup;
+  const int64_t ng = group_slots(vocab);
   return sizeof(Shared) + (size_t)ng * sizeof(float) + (size_t)cap * (sizeof(float) + sizeof(int32_t));
 }
 
-// Candidate-list capacity: up to 8192 entries while two CTAs still fit on an
-// SM, never below 256.
+// Candidate-list capacity: up to 8192 entries while a CTA stays within 96 KB
+// of shared memory, never below 256.  Two such CTAs per SM leave at least
+// 60 KB of the SM's 256 KB L1/shared array to L1, which the streaming loads
+// need for their requests in flight: with 104 KB per CTA a plain 256-row
+// bf16 read of this shape was measured a quarter slower.
 static int cand_capacity(int64_t vocab) {
-  constexpr size_t kTwoPerSm = 112 * 1024;
+  constexpr size_t kPerCta = 96 * 1024;
   const size_t base = smem_bytes(vocab, 0);
   int cap = 8192;
-  while (cap > 256 && base + (size_t)cap * 8 > kTwoPerSm) cap -= 256;
+  while (cap > 256 && base + (size_t)cap * 8 > kPerCta) cap -= 256;
   return cap;
 }
 
