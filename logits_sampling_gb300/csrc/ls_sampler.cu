@@ -731,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     issue(g0 + 3 * STEP, wb);
   }
   // ---- one block reduction: row maximum, total mass, top-k bound --------
+  const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;  // its latency overlaps the reduction
   // Each warp reduces its maximum, rescales every lane's sum to the warp's
   // reference RN(max * c) and adds; after one barrier every warp combines the
   // 16 warp results the same way (fixed order, so S is deterministic and the
@@ -789,7 +790,6 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     const float sq = lane < kWarps && mq > kNegInf ? sh.red_s[lane] * ex2(__fmul_rn(mq, c) - R) : 0.f;
     S = warp_reduce(sq, OpAddF());
   }
-  const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;
   const bool tie_only = greedy || M == kPosInf;  // no temperature-scaled distribution
 
   // ---- total mass when a NaN entry poisoned the online sum ---------------
@@ -930,27 +930,36 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     const unsigned lt = (1u << lane) - 1u;
     const int nchunk = (rv.NG + 127) >> 7;
     int wn = 0;
-    for (int q = tid >> 5; q < nchunk; q += kWarps) {
-      const int g0 = (q << 7) + 4 * lane;
-      float4 m4 = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
-      if (g0 < rv.NG) m4 = *reinterpret_cast<const float4*>(gmax + g0);
-      const bool h0 = m4.x >= lc;
-      const bool h1 = g0 + 1 < rv.NG && m4.y >= lc;
-      const bool h2 = g0 + 2 < rv.NG && m4.z >= lc;
-      const bool h3 = g0 + 3 < rv.NG && m4.w >= lc;
-      const unsigned b0 = __ballot_sync(0xFFFFFFFFu, h0), b1 = __ballot_sync(0xFFFFFFFFu, h1);
-      const unsigned b2 = __ballot_sync(0xFFFFFFFFu, h2), b3 = __ballot_sync(0xFFFFFFFFu, h3);
-      const int tot = __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
-      if (__builtin_expect(wn + tot > kWarpList, 0)) {
-        flush(wn);
-        wn = 0;
+    constexpr int kBatch = 2;  // chunks whose maxima are loaded together
+    for (int q0 = tid >> 5; q0 < nchunk; q0 += kBatch * kWarps) {
+      float4 m4[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int g0 = ((q0 + u * kWarps) << 7) + 4 * lane;
+        m4[u] = g0 < rv.NG ? *reinterpret_cast<const float4*>(gmax + g0)
+                           : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
       }
-      int pos = wn + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
-      if (h0) wl[pos++] = g0;
-      if (h1) wl[pos++] = g0 + 1;
-      if (h2) wl[pos++] = g0 + 2;
-      if (h3) wl[pos] = g0 + 3;
-      wn += tot;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int g0 = ((q0 + u * kWarps) << 7) + 4 * lane;
+        const bool h0 = m4[u].x >= lc;
+        const bool h1 = g0 + 1 < rv.NG && m4[u].y >= lc;
+        const bool h2 = g0 + 2 < rv.NG && m4[u].z >= lc;
+        const bool h3 = g0 + 3 < rv.NG && m4[u].w >= lc;
+        const unsigned b0 = __ballot_sync(0xFFFFFFFFu, h0), b1 = __ballot_sync(0xFFFFFFFFu, h1);
+        const unsigned b2 = __ballot_sync(0xFFFFFFFFu, h2), b3 = __ballot_sync(0xFFFFFFFFu, h3);
+        const int tot = __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+        if (__builtin_expect(wn + tot > kWarpList, 0)) {
+          flush(wn);
+          wn = 0;
+        }
+        int pos = wn + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
+        if (h0) wl[pos++] = g0;
+        if (h1) wl[pos++] = g0 + 1;
+        if (h2) wl[pos++] = g0 + 2;
+        if (h3) wl[pos] = g0 + 3;
+        wn += tot;
+      }
     }
     flush(wn);
     __syncthreads();
