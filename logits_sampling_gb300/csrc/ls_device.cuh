@@ -194,6 +194,18 @@ __device__ __forceinline__ T block_reduce(T v, Op op, T* red) {
   return r;
 }
 
+// Warp-wide max / min of a float in one instruction (NaN inputs ignored).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float warp_min(float v) {
+  float r;
+  asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 struct OpMax {
   __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
 };

@@ -59,6 +59,7 @@ struct KernelArgs {
 };
 
 constexpr int kWarpList = 128;  // candidate groups a warp lists before loading them
+constexpr int kTieList = 32;    // ties of the maximum recorded while collecting
 
 // Group-maximum slots of a row: worst-case row alignment, rounded up to whole
 // 16-byte vectors so that the maxima can be scanned four at a time.
@@ -82,6 +83,8 @@ struct alignas(16) Shared {
   int cut_bin;
   int min_index;
   int cand_count;
+  int tie_count;        // ties of the maximum met while collecting
+  int tie_j[kTieList];  // their vocabulary indices (the first kTieList)
   int glist[kWarps * kWarpList];  // candidate group indices, one slice per warp
   float red_m[kWarps];
   float red_s[kWarps];
@@ -490,9 +493,12 @@ __device__ __forceinline__ unsigned long long find_cut_bin(Shared& sh, int nb, u
                                                            const W& weight) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int top = nb - 1 - t * kBinsPerThread;
-  unsigned long long local = 0;
+  unsigned long long w[kBinsPerThread], local = 0;
 #pragma unroll
-  for (int q = 0; q < kBinsPerThread; ++q) local += top - q >= 0 ? weight(top - q) : 0ull;
+  for (int q = 0; q < kBinsPerThread; ++q) {
+    w[q] = top - q >= 0 ? weight(top - q) : 0ull;
+    local += w[q];
+  }
   unsigned long long incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -513,15 +519,15 @@ __device__ __forceinline__ unsigned long long find_cut_bin(Shared& sh, int nb, u
   if (target < 1ull) target = 1ull;
   unsigned long long cum = above + base + incl - local;
   if (cum < target && cum + local >= target) {
-    for (int q = 0; q < kBinsPerThread; ++q) {  // one thread: weights taken again
-      const unsigned long long wq = weight(top - q);
-      if (cum + wq >= target) {
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+      if (cum + w[q] >= target) {
         sh.cut_bin = top - q;
         sh.cut_above = cum;
-        sh.cut_mass = wq;
+        sh.cut_mass = w[q];
         break;
       }
-      cum += wq;
+      cum += w[q];
     }
   }
   __syncthreads();
@@ -745,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   }
   const int lane = tid & 31;
   {
-    const float mw = warp_reduce(m, OpMax());
+    const float mw = warp_max(m);
     float sw = 0.f;
     if (need_sum && mw > kNegInf) {
       float lo, hi;
@@ -758,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       const int jrank = (k + kWarps - 1) / kWarps;
       float cur = m;
       for (int t = 0; t < jrank; ++t) {
-        gj = warp_reduce(cur, OpMax());
+        gj = warp_max(cur);
         const unsigned holders = __ballot_sync(0xFFFFFFFFu, cur == gj);
         if (lane == __ffs(holders) - 1) cur = kNegInf;
       }
@@ -775,11 +781,12 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     sh.acc[1] = 0u;
     sh.min_index = 0x7FFFFFFF;
     sh.cand_count = 0;
+    sh.tie_count = 0;
   }
   __syncthreads();
   const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
-  const float M = warp_reduce(mq, OpMax());
-  const float gamma = warp_reduce(lane < kWarps ? sh.red_f[lane] : kPosInf, OpMin());
+  const float M = warp_max(mq);
+  const float gamma = warp_min(lane < kWarps ? sh.red_f[lane] : kPosInf);
   if (M == kNegInf) {
     row_error(a, i, MODE, LS_ROW_ERR_NO_FINITE);
     return;
@@ -852,9 +859,8 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // (two per lane per round, all loads in flight at once) and takes their
   // entries >= lc: they are appended to the shared-memory candidate list (one
   // atomic per warp and round), feed the first select level's histogram and,
-  // when sampling, the maximum's ties get their exact Gumbel score (the best
-  // is a lower bound of the winner's score).  No block barrier until every
-  // warp is done.
+  // when sampling, the maximum's ties are recorded.  No block barrier until
+  // every warp is done.
   using RVT = RowView<TIn>;
   int count = 0;
   // Entry >= lc of a loaded group: append it to the list and feed the first
@@ -880,7 +886,10 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
             atomicAdd(&sh.hist[bin], 1u);
         }
       }
-      if (ties_in_take && x >= M) score_entry(&sh.best, x, T, seed, a.step, (uint32_t)i, rv.index(g, e));
+      if (ties_in_take && x >= M) {
+        const int q = atomicAdd(&sh.tie_count, 1);
+        if (q < kTieList) sh.tie_j[q] = (int)rv.index(g, e);
+      }
     }
   };
   if (lc <= M) {
@@ -967,10 +976,15 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   }
   const Cands<TIn> cs{&rv, gmax, cand_v, cand_j, count, lc <= M && count <= a.cand_cap};
 
-  // The maximum's ties, unless collecting already scored them: lowest index
-  // (greedy), count (log-probs of ties-only rows) or exact Gumbel score
-  // (sampling; the best is a lower bound of the winner's score).
-  if (tie_only || (MODE == MODE_SAMPLE && !(lc <= M))) {
+  // The maximum's ties: lowest index (greedy), count (log-probs of ties-only
+  // rows) or exact Gumbel score (sampling; the best is a lower bound of the
+  // winner's score).  Sampling rows that collected candidates recorded their
+  // ties there: one thread scores each (sh.best is next read after the cut's
+  // barriers); only more than kTieList ties take a pass over the list.
+  const int nties = ties_in_take && lc <= M ? sh.tie_count : -1;
+  if (nties >= 0 && nties <= kTieList) {
+    if (tid < nties) score_entry(&sh.best, M, T, seed, a.step, (uint32_t)i, sh.tie_j[tid]);
+  } else if (tie_only || MODE == MODE_SAMPLE) {
     cs.each(M, [&](float x, int64_t j) {
       if (MODE == MODE_LOGPROBS) {
         atomicAdd(&sh.acc[0], 1u);
