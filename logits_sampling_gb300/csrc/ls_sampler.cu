@@ -62,7 +62,7 @@ constexpr int kWarpList = 128;  // candidate groups a warp lists before loading 
 constexpr int kTieList = 32;    // ties of the maximum recorded while collecting
 
 // Group-maximum slots of a row: worst-case row alignment, rounded up to whole
-// 16-byte vectors so that the maxima can be scanned four at a time.
+// 16-byte vectors (the candidate list that follows stays 16-byte aligned).
 __host__ __device__ inline int64_t group_slots(int64_t vocab) {
   return ((vocab + 2 * kGroup - 1) / kGroup + 3) & ~(int64_t)3;
 }
@@ -936,41 +936,39 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       }
       __syncwarp();
     };
-    const unsigned lt = (1u << lane) - 1u;
-    const int nchunk = (rv.NG + 127) >> 7;
-    int wn = 0;
-    constexpr int kBatch = 2;  // chunks whose maxima are loaded together
-    for (int q0 = tid >> 5; q0 < nchunk; q0 += kBatch * kWarps) {
-      float4 m4[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int g0 = ((q0 + u * kWarps) << 7) + 4 * lane;
-        m4[u] = g0 < rv.NG ? *reinterpret_cast<const float4*>(gmax + g0)
-                           : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+    // Each thread tests the maxima of its own groups (tid + 512 s, the ones
+    // it streamed), 32 slots at a time; one warp prefix over the per-thread
+    // counts places the candidate groups in the warp's list slice, which is
+    // loaded and taken kWarpList groups at a time.
+    const int nslots = (rv.NG + kThreads - 1) / kThreads;
+    for (int sb = 0; sb < nslots; sb += 32) {
+      const int send = min(32, nslots - sb);
+      uint32_t mask = 0u;
+#pragma unroll 8
+      for (int q = 0; q < send; ++q) {
+        const int g = tid + (sb + q) * kThreads;
+        if (g < rv.NG && gmax[g] >= lc) mask |= 1u << q;
       }
+      const int cnt = __popc(mask);
+      int incl = cnt;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int g0 = ((q0 + u * kWarps) << 7) + 4 * lane;
-        const bool h0 = m4[u].x >= lc;
-        const bool h1 = g0 + 1 < rv.NG && m4[u].y >= lc;
-        const bool h2 = g0 + 2 < rv.NG && m4[u].z >= lc;
-        const bool h3 = g0 + 3 < rv.NG && m4[u].w >= lc;
-        const unsigned b0 = __ballot_sync(0xFFFFFFFFu, h0), b1 = __ballot_sync(0xFFFFFFFFu, h1);
-        const unsigned b2 = __ballot_sync(0xFFFFFFFFu, h2), b3 = __ballot_sync(0xFFFFFFFFu, h3);
-        const int tot = __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
-        if (__builtin_expect(wn + tot > kWarpList, 0)) {
-          flush(wn);
-          wn = 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t2;
+      }
+      const int wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      for (int w0 = 0; w0 < wtot; w0 += kWarpList) {
+        uint32_t mm = mask;
+        int at = incl - cnt;
+        while (mm) {
+          const int q = __ffs(mm) - 1;
+          mm &= mm - 1u;
+          if (at >= w0 && at < w0 + kWarpList) wl[at - w0] = tid + (sb + q) * kThreads;
+          ++at;
         }
-        int pos = wn + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
-        if (h0) wl[pos++] = g0;
-        if (h1) wl[pos++] = g0 + 1;
-        if (h2) wl[pos++] = g0 + 2;
-        if (h3) wl[pos] = g0 + 3;
-        wn += tot;
+        flush(min(kWarpList, wtot - w0));
       }
     }
-    flush(wn);
     __syncthreads();
     count = sh.cand_count;
   }
