@@ -183,6 +183,10 @@ struct RowView<bf16_tag> {
     }
     return m;
   }
+  // Entry e of the group for an index known at compile time.
+  __device__ __forceinline__ static float element_at(const uint32_t (&w)[kWords], int e) {
+    return __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+  }
   // Entry e of the group (a select chain, so the words stay in registers).
   __device__ __forceinline__ static float element(const uint32_t (&w)[kWords], int e) {
     uint32_t word = w[0];
@@ -274,6 +278,9 @@ struct RowView<float> {
 #pragma unroll
     for (int q = 0; q < kWords; ++q) m |= (__uint_as_float(w[q]) >= lo ? 1u : 0u) << q;
     return m;
+  }
+  __device__ __forceinline__ static float element_at(const uint32_t (&w)[kWords], int e) {
+    return __uint_as_float(w[e]);
   }
   __device__ __forceinline__ static float element(const uint32_t (&w)[kWords], int e) {
     uint32_t word = w[0];
@@ -436,22 +443,79 @@ __device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float l
       if (v >= lo2 && v < M) test(v, (int64_t)cs.lj[q]);
     }
   } else {
-    // candidate groups re-read from global memory, entries of a group in order
+    // Candidate groups re-read from global memory (normally L2), the next
+    // one in flight while the current one is tested.  An interior group
+    // whose first index is a multiple of 4 spans exactly four Philox blocks:
+    // they are drawn together (four independent chains), and a group-level
+    // threshold taken at the group's largest z rejects most entries with one
+    // integer compare of their uniform; survivors take the exact test.
     const RowView<TIn>& rv = *cs.rv;
-    for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
-      if (!(cs.gmax[g] >= lo2)) continue;
-      uint32_t w[RVT::kWords];
+    const uint2 key = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+    auto next = [&](int g) {
+      while (g < rv.NG && !(cs.gmax[g] >= lo2)) g += kThreads;
+      return g;
+    };
+    auto load = [&](int g, uint32_t (&w)[RVT::kWords]) {
       if (rv.full(g))
         rv.load_words(g, w);
       else
         rv.load_words_partial(g, w);
-      uint32_t mm = RVT::ge_mask(w, lo2);
+    };
+    constexpr bool kAhead = RVT::kWords <= 8;  // next group in flight (bf16: registers allow it)
+    int g = next(threadIdx.x);
+    uint32_t w[RVT::kWords];
+    if (kAhead && g < rv.NG) load(g, w);
+    while (g < rv.NG) {
+      const int gn = next(g + kThreads);
+      uint32_t wn[RVT::kWords];
+      if (kAhead) {
+        if (gn < rv.NG) load(gn, wn);
+      } else {
+        load(g, w);
+      }
+      const int64_t j0 = rv.index(g, 0);
+      if (rv.full(g) && (j0 & 3) == 0) {
+        // every entry of the group has z <= fl(gmax / T): its threshold is at
+        // least the group's, so u below the group's threshold rejects it
+        const float zg = __fdiv_rn(cs.gmax[g], T);
+        const float need_g = s_lb - zg - 1e-3f;
+        const float thr_g = ex2(-ex2(-need_g * kLog2e) * kLog2e) * (1.f - 4e-7f);
+        // u = (2 (x >> 9) + 1) 2^-24 >= thr_g  implies  2 (x >> 9) + 1 >= floor(thr_g 2^24)
+        const uint32_t thr_i = (uint32_t)(thr_g * 16777216.f);
+        const uint32_t b0 = (uint32_t)((uint64_t)j0 >> 2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // two blocks (eight entries) at a time
+          const uint4 p0 = philox4x32_10(make_uint4(b0 + 2 * h, row, (uint32_t)step, (uint32_t)(step >> 32)), key);
+          const uint4 p1 = philox4x32_10(make_uint4(b0 + 2 * h + 1, row, (uint32_t)step, (uint32_t)(step >> 32)), key);
+#pragma unroll
+          for (int e8 = 0; e8 < 8; ++e8) {
+            const int e = 8 * h + e8;
+            const uint4 bq = e8 < 4 ? p0 : p1;
+            const uint32_t x = (e & 3) == 0 ? bq.x : (e & 3) == 1 ? bq.y : (e & 3) == 2 ? bq.z : bq.w;
+            const float v = RVT::element_at(w, e);
+            if (v >= lo2 && v < M && (((x >> 9) << 1) | 1u) >= thr_i) {
+              const float z = __fdiv_rn(v, T);
+              const float need = s_lb - z - 1e-3f;
+              const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
+              const float u = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
+              if (u >= thr) atomicMax(&sh.best, argmax_key(z + gumbel_of_word(x), j0 + e));
+            }
+          }
+        }
+      } else {
+        uint32_t mm = RVT::ge_mask(w, lo2);
 #pragma unroll 1
-      while (mm) {
-        const int e = __ffs(mm) - 1;
-        mm &= mm - 1u;
-        const float v = RVT::element(w, e);
-        if (v < M) test(v, rv.index(g, e));
+        while (mm) {
+          const int e = __ffs(mm) - 1;
+          mm &= mm - 1u;
+          const float v = RVT::element(w, e);
+          if (v < M) test(v, rv.index(g, e));
+        }
+      }
+      g = gn;
+      if (kAhead) {
+#pragma unroll
+        for (int q = 0; q < RVT::kWords; ++q) w[q] = wn[q];
       }
     }
   }
