@@ -44,18 +44,35 @@ def up_to_date():
 
 
 def build(force=False, verbose=False):
-    """Compile the shared library; returns its path."""
+    """Compile the shared library; returns its path.  Each translation unit
+    (one per kernel mode, plus the C ABI) compiles in its own nvcc process, in
+    parallel; the objects are then linked."""
     if not force and up_to_date():
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-I", INCLUDE, "-I", CSRC, *sources(), "-o", tmp, "-lcudart"]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd))
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    objs, procs = [], []
+    for src in sources():
+        obj = os.path.join(PKG, os.path.basename(src)[:-3] + tag + ".o")
+        cmd = [_nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+               "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+            print(" ".join(cmd))
+        objs.append(obj)
+        procs.append(subprocess.Popen(cmd))
+    failed = [p.args[-3] for p in procs if p.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, "nvcc", f"compiling {failed} failed")
+        tmp = LIB + tag
+        subprocess.run([_nvcc(), *ARCH_FLAGS, "-shared", *objs, "-o", tmp, "-lcudart"], check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB
+
 
 
 if __name__ == "__main__":

@@ -1,0 +1,1219 @@
+#pragma once
+// ls_kernel.cuh -- GB300 (sm_103a) kernel of the token sampler and its
+// host-side launch helpers.  Each ls_mode_*.cu instantiates `dispatch` for one
+// mode (so the modes compile in parallel); ls_sampler.cu holds the C ABI.
+//
+// One CTA of 512 threads owns one sampled row.  The row is read from HBM once,
+// with 256-bit loads, by a single streaming pass that keeps, per group of 16
+// logits, the group maximum in shared memory and, per thread, a running
+// maximum and (when the row needs it) the online sum of exp((l - max) / T).
+// Everything after that pass touches only candidate groups -- groups whose
+// maximum clears a provable lower bound of what can be kept or sampled -- and
+// re-reads them from L2:
+//   * exact top-k cut: an adaptive 11-bit radix select on order-preserving keys;
+//   * exact top-p cut: the same select weighted by fixed-point masses
+//     (deterministic 64-bit integer atomics), joint = top-k cut first;
+//   * Gumbel-max over the kept set with in-register Philox4x32-10 noise, only
+//     for entries within the noise span of the row maximum.
+// The log-probs kernel runs the same selection and then writes the full
+// [vocab] row of log-probs.
+//
+// The behaviour follows "core.inference.sampling.base" (Sampling.sample_kernel,
+// Sampling.sample_speculative), "core.inference.sampling.flashinfer_sampling"
+// (FlashInferSampling: per-step top-p-only / top-k-only / joint dispatch from
+// host flags, log_probs_kernel) and the TokenSpeed "backends/triton.py" page
+// (TritonSamplingBackend: Gumbel-max sampling from per-request pools).
+
+#include <atomic>
+#include <cfloat>
+#include <cstdint>
+#include <cstdio>
+#include <cuda_runtime.h>
+
+#include "ls_device.cuh"
+#include "ls_sampler.h"
+
+namespace lsg {
+
+enum MapMode { MAP_IDENTITY = 0, MAP_T2R = 1, MAP_SPEC = 2 };
+enum Mode { MODE_SAMPLE = 0, MODE_LOGPROBS = 1 };
+enum Route { ROUTE_NONE = 0, ROUTE_K = 1, ROUTE_P = 2, ROUTE_KP = 3 };
+
+struct KernelArgs {
+  const void* logits;
+  int64_t logits_rows, vocab, stride;
+  const int32_t* gather;
+  const int32_t* t2r;
+  int map_mode;
+  int32_t spec_decode_rows;  // num_decode * (1 + S)
+  int32_t spec_per_req;      // 1 + S
+  int32_t spec_num_decode;
+  const float* temperature;
+  const int32_t* top_k;
+  const float* top_p;
+  const uint64_t* seed;
+  int32_t num_requests;
+  uint64_t step;
+  int32_t* out_ids;
+  int32_t* out_t2r;
+  float* out_lp;
+  int32_t* error_word;
+  int32_t cand_cap;  // capacity of the shared-memory candidate list
+};
+
+constexpr int kWarpList = 128;  // candidate groups a warp lists before loading them
+constexpr int kTieList = 32;    // ties of the maximum recorded while collecting
+
+// Group-maximum slots of a row: worst-case row alignment, rounded up to whole
+// 16-byte vectors (the candidate list that follows stays 16-byte aligned).
+__host__ __device__ inline int64_t group_slots(int64_t vocab) {
+  return ((vocab + 2 * kGroup - 1) / kGroup + 3) & ~(int64_t)3;
+}
+
+// Fixed part of the dynamic shared memory; the group maxima follow it.
+struct alignas(16) Shared {
+  // Histogram: u32 counts, or masses as (lo, hi) u32 pairs updated with
+  // carry-propagating 32-bit atomics (shared-memory 64-bit adds are not
+  // native and degrade badly under contention).
+  unsigned int hist[2 * kBins];
+  unsigned long long red_u64[kWarps];
+  float red_f[kWarps];
+  int red_i[kWarps];
+  unsigned long long best;
+  unsigned int acc[2];  // a count in acc[0], or a mass as a (lo, hi) pair
+  unsigned long long cut_above;
+  unsigned long long cut_mass;
+  int cut_bin;
+  int min_index;
+  int cand_count;
+  int tie_count;        // ties of the maximum met while collecting
+  int tie_j[kTieList];  // their vocabulary indices (the first kTieList)
+  int glist[kWarps * kWarpList];  // candidate group indices, one slice per warp
+  float red_m[kWarps];
+  float red_s[kWarps];
+};
+
+// Exact 64-bit add into a (lo, hi) pair of u32 counters with two native
+// 32-bit atomics: the thread whose addition wraps the low word carries one
+// into the high word, so the pair ends at the exact sum in any order.
+__device__ __forceinline__ void add_mass(unsigned int* pair, unsigned long long w) {
+  const unsigned int lo = (unsigned int)w, hi = (unsigned int)(w >> 32);
+  const unsigned int old = atomicAdd(pair, lo);
+  const unsigned int carry = (old + lo < old) ? 1u : 0u;
+  if (hi + carry) atomicAdd(pair + 1, hi + carry);
+}
+__device__ __forceinline__ unsigned long long read_mass(const unsigned int* pair) {
+  return ((unsigned long long)pair[1] << 32) | pair[0];
+}
+
+// round(w * 2^40) for a weight w in [0, 1], from the float's bits with integer
+// operations only (64-bit float/integer conversions run on the slow FP64
+// pipe).  Weights below 2^-41 give 0.
+__device__ __forceinline__ unsigned long long mass_fixed(float w) {
+  const uint32_t b = __float_as_uint(w);
+  const int e = (int)((b >> 23) & 0xFFu);
+  if (e == 0) return 0ull;
+  const unsigned long long mant = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 110;  // w * 2^40 = mant * 2^(e - 127 - 23 + 40)
+  if (sh >= 0) return mant << sh;
+  if (sh <= -25) return 0ull;
+  return (mant + (1ull << (-sh - 1))) >> (-sh);
+}
+
+// ---------------------------------------------------------------------------
+// Row view: groups of 16 logits aligned to the group size in bytes, so that
+// every interior group is one (bf16) or two (fp32) aligned 256-bit loads.
+// Group g covers row entries [16 g - off, 16 g - off + 16); entries outside
+// [0, vocab) read as -inf.
+// ---------------------------------------------------------------------------
+template <typename TIn>
+struct RowView;
+
+__device__ __forceinline__ void ld256(const void* p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+template <>
+struct RowView<bf16_tag> {
+  static constexpr int kBytes = 2;
+  const uint16_t* row;
+  const unsigned char* base;  // group 0, aligned to 32 bytes
+  int off;
+  int64_t V;
+  int NG;
+  __device__ __forceinline__ void init(const void* logits, int64_t src, int64_t stride, int64_t vocab) {
+    row = static_cast<const uint16_t*>(logits) + src * stride;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    base = reinterpret_cast<const unsigned char*>(a & ~uintptr_t(31));
+    off = (int)((a - reinterpret_cast<uintptr_t>(base)) / 2);
+    V = vocab;
+    NG = (int)((off + vocab + kGroup - 1) / kGroup);
+    g_full_lo = off > 0 ? 1 : 0;
+    g_full_hi = (int)((off + vocab) / kGroup) - 1;
+  }
+  int g_full_lo, g_full_hi;  // groups lying entirely inside the row
+  __device__ __forceinline__ int64_t index(int g, int e) const { return (int64_t)g * kGroup - off + e; }
+  static constexpr int kWords = 8;
+  // Raw words of a group that straddles the row's ends; outside entries read as -inf.
+  __device__ __forceinline__ void load_words_partial(int g, uint32_t (&w)[kWords]) const {
+    const int64_t j0 = index(g, 0);
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) {
+      const int64_t a = j0 + 2 * q, b = a + 1;
+      const uint32_t lo = (a >= 0 && a < V) ? (uint32_t)row[a] : 0xFF80u;
+      const uint32_t hi = (b >= 0 && b < V) ? (uint32_t)row[b] : 0xFF80u;
+      w[q] = lo | (hi << 16);
+    }
+  }
+  // Maximum of the 16 entries (NaN ignored unless all are NaN).
+  __device__ __forceinline__ static float group_max(const uint32_t (&w)[kWords]) {
+    const uint32_t a = bmax2(bmax2(w[0], w[1]), bmax2(w[2], w[3]));
+    const uint32_t b = bmax2(bmax2(w[4], w[5]), bmax2(w[6], w[7]));
+    const uint32_t m = bmax2(a, b);
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  }
+  // Bit e set when entry e is >= lo (NaN never).
+  __device__ __forceinline__ static uint32_t ge_mask(const uint32_t (&w)[kWords], float lo) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) {
+      m |= (__uint_as_float(w[q] << 16) >= lo ? 1u : 0u) << (2 * q);
+      m |= (__uint_as_float(w[q] & 0xFFFF0000u) >= lo ? 1u : 0u) << (2 * q + 1);
+    }
+    return m;
+  }
+  // Entry e of the group for an index known at compile time.
+  __device__ __forceinline__ static float element_at(const uint32_t (&w)[kWords], int e) {
+    return __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+  }
+  // Entry e of the group (a select chain, so the words stay in registers).
+  __device__ __forceinline__ static float element(const uint32_t (&w)[kWords], int e) {
+    uint32_t word = w[0];
+#pragma unroll
+    for (int q = 1; q < kWords; ++q) word = select_word(word, w[q], (e >> 1) == q);
+    return __uint_as_float((e & 1) ? (word & 0xFFFF0000u) : (word << 16));
+  }
+  // Packed partial sums of 2^(v c - r) over the 16 entries.
+  __device__ __forceinline__ static f32x2 exp_sum(const uint32_t (&w)[kWords], f32x2 c2, f32x2 nr2) {
+    f32x2 s0 = 0ull, s1 = 0ull;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) {
+      const f32x2 t = fma2(pack2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u)), c2, nr2);
+      float t0, t1;
+      unpack2(t, t0, t1);
+      const f32x2 e = pack2(ex2(t0), ex2(t1));
+      if (q & 1)
+        s1 = add2(s1, e);
+      else
+        s0 = add2(s0, e);
+    }
+    return add2(s0, s1);
+  }
+  __device__ __forceinline__ float at(int64_t j) const { return bf16_bits_to_float(row[j]); }
+  __device__ __forceinline__ bool full(int g) const { return g >= g_full_lo && g <= g_full_hi; }
+  __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords]) const { ld256(base + (size_t)g * 32, w); }
+  __device__ __forceinline__ static void unpack(const uint32_t (&w)[kWords], float (&v)[kGroup]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  }
+  __device__ __forceinline__ void load(int g, float (&v)[kGroup]) const {
+    const int64_t j0 = index(g, 0);
+    if (j0 >= 0 && j0 + kGroup <= V) {
+      uint32_t r[kWords];
+      load_words(g, r);
+      unpack(r, v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e) {
+        const int64_t j = j0 + e;
+        v[e] = (j >= 0 && j < V) ? at(j) : kNegInf;
+      }
+    }
+  }
+};
+
+template <>
+struct RowView<float> {
+  static constexpr int kBytes = 4;
+  const float* row;
+  const unsigned char* base;  // group 0, aligned to 64 bytes
+  int off;
+  int64_t V;
+  int NG;
+  __device__ __forceinline__ void init(const void* logits, int64_t src, int64_t stride, int64_t vocab) {
+    row = static_cast<const float*>(logits) + src * stride;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    base = reinterpret_cast<const unsigned char*>(a & ~uintptr_t(63));
+    off = (int)((a - reinterpret_cast<uintptr_t>(base)) / 4);
+    V = vocab;
+    NG = (int)((off + vocab + kGroup - 1) / kGroup);
+    g_full_lo = off > 0 ? 1 : 0;
+    g_full_hi = (int)((off + vocab) / kGroup) - 1;
+  }
+  int g_full_lo, g_full_hi;  // groups lying entirely inside the row
+  __device__ __forceinline__ int64_t index(int g, int e) const { return (int64_t)g * kGroup - off + e; }
+  static constexpr int kWords = 16;
+  __device__ __forceinline__ void load_words_partial(int g, uint32_t (&w)[kWords]) const {
+    const int64_t j0 = index(g, 0);
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) {
+      const int64_t j = j0 + q;
+      w[q] = (j >= 0 && j < V) ? __float_as_uint(row[j]) : 0xFF800000u;
+    }
+  }
+  __device__ __forceinline__ static float group_max(const uint32_t (&w)[kWords]) {
+    float v[kGroup];
+#pragma unroll
+    for (int q = 0; q < kGroup; ++q) v[q] = __uint_as_float(w[q]);
+    const float a = fmax3(v[0], v[1], v[2]), b = fmax3(v[3], v[4], v[5]), c = fmax3(v[6], v[7], v[8]);
+    const float d = fmax3(v[9], v[10], v[11]), e = fmax3(v[12], v[13], v[14]);
+    return fmaxf(fmax3(a, b, c), fmax3(d, e, v[15]));
+  }
+  __device__ __forceinline__ static uint32_t ge_mask(const uint32_t (&w)[kWords], float lo) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int q = 0; q < kWords; ++q) m |= (__uint_as_float(w[q]) >= lo ? 1u : 0u) << q;
+    return m;
+  }
+  __device__ __forceinline__ static float element_at(const uint32_t (&w)[kWords], int e) {
+    return __uint_as_float(w[e]);
+  }
+  __device__ __forceinline__ static float element(const uint32_t (&w)[kWords], int e) {
+    uint32_t word = w[0];
+#pragma unroll
+    for (int q = 1; q < kWords; ++q) word = select_word(word, w[q], e == q);
+    return __uint_as_float(word);
+  }
+  __device__ __forceinline__ static f32x2 exp_sum(const uint32_t (&w)[kWords], f32x2 c2, f32x2 nr2) {
+    f32x2 s0 = 0ull, s1 = 0ull;
+#pragma unroll
+    for (int q = 0; q < kWords / 2; ++q) {
+      const f32x2 t = fma2(pack2(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1])), c2, nr2);
+      float t0, t1;
+      unpack2(t, t0, t1);
+      const f32x2 e = pack2(ex2(t0), ex2(t1));
+      if (q & 1)
+        s1 = add2(s1, e);
+      else
+        s0 = add2(s0, e);
+    }
+    return add2(s0, s1);
+  }
+  __device__ __forceinline__ float at(int64_t j) const { return row[j]; }
+  __device__ __forceinline__ bool full(int g) const { return g >= g_full_lo && g <= g_full_hi; }
+  __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords]) const {
+    ld256(base + (size_t)g * 64, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
+    ld256(base + (size_t)g * 64 + 32, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
+  }
+  __device__ __forceinline__ static void unpack(const uint32_t (&w)[kWords], float (&v)[kGroup]) {
+#pragma unroll
+    for (int q = 0; q < kGroup; ++q) v[q] = __uint_as_float(w[q]);
+  }
+  __device__ __forceinline__ void load(int g, float (&v)[kGroup]) const {
+    const int64_t j0 = index(g, 0);
+    if (j0 >= 0 && j0 + kGroup <= V) {
+      uint32_t r[kWords];
+      load_words(g, r);
+      unpack(r, v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e) {
+        const int64_t j = j0 + e;
+        v[e] = (j >= 0 && j < V) ? at(j) : kNegInf;
+      }
+    }
+  }
+};
+
+template <typename TIn>
+struct KeyOf {
+  using type = KeyOps<TIn>;
+};
+
+__device__ __forceinline__ float max16(const float (&v)[kGroup]) {
+  float a = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+  float b = fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7]));
+  float c = fmaxf(fmaxf(v[8], v[9]), fmaxf(v[10], v[11]));
+  float d = fmaxf(fmaxf(v[12], v[13]), fmaxf(v[14], v[15]));
+  return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
+// Visit every row entry whose value is >= lo (NaN never qualifies), looking
+// only at groups whose maximum is >= lo.  Candidate groups are re-read from
+// global memory (normally still in L2 after the streaming pass).
+template <typename TIn, typename F>
+__device__ __forceinline__ void visit_candidates(const RowView<TIn>& rv, const float* gmax, float lo, F&& f) {
+  for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
+    if (gmax[g] >= lo) {
+      float v[kGroup];
+      rv.load(g, v);
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e)
+        if (v[e] >= lo) f(v[e], rv.index(g, e));
+    }
+  }
+}
+
+// The row entries that later phases examine.  After the streaming pass one
+// visit of the candidate groups copies every entry >= the row's candidate
+// bound into a shared-memory list (value, index); all later phases then read
+// that list.  If the list would overflow, phases fall back to re-reading the
+// candidate groups from global memory.
+template <typename TIn>
+struct Cands {
+  const RowView<TIn>* rv;
+  const float* gmax;
+  const float* lv;    // values
+  const int32_t* lj;  // vocabulary indices
+  int count;
+  bool listed;
+  template <typename F>
+  __device__ __forceinline__ void each(float lo, F&& f) const {
+    if (listed) {
+      for (int c = threadIdx.x; c < count; c += kThreads) {
+        const float v = lv[c];
+        if (v >= lo) f(v, (int64_t)lj[c]);
+      }
+    } else {
+      visit_candidates(*rv, gmax, lo, f);
+    }
+  }
+};
+
+// Gumbel-max over the kept entries with value >= lo, given in sh.best the
+// exact score of the best of the maximum's ties (always kept): s_lb, a lower
+// bound of the winner's score.  Only entries with z >= s_lb - 16.6356 can
+// still win (g <= 16.6356); of those, an entry needs g >= s_lb - z, i.e.
+// u >= exp(-exp(z - s_lb)).  That test (taken 1e-3 looser in g) runs on the
+// Philox word alone, and only entries passing it compute the two logarithms.
+// Leaves the winner's key in sh.best.
+// One Philox block yields the noise words of four consecutive vocabulary
+// entries; a thread walking consecutive entries reuses it.
+struct PhiloxCache {
+  uint32_t id = 0xFFFFFFFFu;
+  uint4 blk = make_uint4(0u, 0u, 0u, 0u);
+  __device__ __forceinline__ uint32_t word(uint64_t seed, uint64_t step, uint32_t row, int64_t j) {
+    const uint32_t b = (uint32_t)((uint64_t)j >> 2);
+    if (b != id) {
+      id = b;
+      blk = philox4x32_10(make_uint4(b, row, (uint32_t)step, (uint32_t)(step >> 32)),
+                          make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+    }
+    const uint32_t ln = (uint32_t)j & 3u;
+    return ln == 0 ? blk.x : ln == 1 ? blk.y : ln == 2 ? blk.z : blk.w;
+  }
+};
+
+// Exact Gumbel score of entry j (value x) raised into *best.
+__device__ __forceinline__ void score_entry(unsigned long long* best, float x, float T, uint64_t seed, uint64_t step,
+                                         uint32_t row, int64_t j) {
+  atomicMax(best, argmax_key(__fdiv_rn(x, T) + gumbel_of_word(noise_word(seed, step, row, j)), j));
+}
+
+template <typename TIn>
+__device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float lo, float T, uint64_t seed,
+                              uint64_t step, uint32_t row) {
+  using RVT = RowView<TIn>;
+  const float s_lb = f32_from_key((uint32_t)(sh.best >> 32));
+  // z >= s_lb - 16.6356, in logit units (T > 0), lowered by a rounding margin
+  float lb = (s_lb - 16.6366f) * T;
+  lb -= fabsf(lb) * 1e-5f + 1e-30f;
+  const float lo2 = fmaxf(lo, lb);
+  PhiloxCache pc;
+  auto test = [&](float v, int64_t j) {
+    const float z = __fdiv_rn(v, T);
+    const float need = s_lb - z - 1e-3f;
+    const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
+    const uint32_t x = pc.word(seed, step, row, j);
+    const float u = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
+    if (u >= thr) atomicMax(&sh.best, argmax_key(z + gumbel_of_word(x), j));
+  };
+  if (cs.listed) {
+    // each thread walks a contiguous run of the list (entries of one group are
+    // consecutive there), so neighbouring entries share Philox blocks
+    const int per = (cs.count + kThreads - 1) / kThreads;
+    const int c0 = threadIdx.x * per, c1 = min(cs.count, c0 + per);
+#pragma unroll 1
+    for (int q = c0; q < c1; ++q) {
+      const float v = cs.lv[q];
+      if (v >= lo2 && v < M) test(v, (int64_t)cs.lj[q]);
+    }
+  } else {
+    // Candidate groups re-read from global memory (normally L2), the next
+    // one in flight while the current one is tested.  An interior group
+    // whose first index is a multiple of 4 spans exactly four Philox blocks:
+    // they are drawn together (four independent chains), and a group-level
+    // threshold taken at the group's largest z rejects most entries with one
+    // integer compare of their uniform; survivors take the exact test.
+    const RowView<TIn>& rv = *cs.rv;
+    const uint2 key = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+    auto next = [&](int g) {
+      while (g < rv.NG && !(cs.gmax[g] >= lo2)) g += kThreads;
+      return g;
+    };
+    auto load = [&](int g, uint32_t (&w)[RVT::kWords]) {
+      if (rv.full(g))
+        rv.load_words(g, w);
+      else
+        rv.load_words_partial(g, w);
+    };
+    constexpr bool kAhead = RVT::kWords <= 8;  // next group in flight (bf16: registers allow it)
+    int g = next(threadIdx.x);
+    uint32_t w[RVT::kWords];
+    if (kAhead && g < rv.NG) load(g, w);
+    while (g < rv.NG) {
+      const int gn = next(g + kThreads);
+      uint32_t wn[RVT::kWords];
+      if (kAhead) {
+        if (gn < rv.NG) load(gn, wn);
+      } else {
+        load(g, w);
+      }
+      const int64_t j0 = rv.index(g, 0);
+      if (rv.full(g) && (j0 & 3) == 0) {
+        // every entry of the group has z <= fl(gmax / T): its threshold is at
+        // least the group's, so u below the group's threshold rejects it
+        const float zg = __fdiv_rn(cs.gmax[g], T);
+        const float need_g = s_lb - zg - 1e-3f;
+        const float thr_g = ex2(-ex2(-need_g * kLog2e) * kLog2e) * (1.f - 4e-7f);
+        // u = (2 (x >> 9) + 1) 2^-24 >= thr_g  implies  2 (x >> 9) + 1 >= floor(thr_g 2^24)
+        const uint32_t thr_i = (uint32_t)(thr_g * 16777216.f);
+        const uint32_t b0 = (uint32_t)((uint64_t)j0 >> 2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // two blocks (eight entries) at a time
+          const uint4 p0 = philox4x32_10(make_uint4(b0 + 2 * h, row, (uint32_t)step, (uint32_t)(step >> 32)), key);
+          const uint4 p1 = philox4x32_10(make_uint4(b0 + 2 * h + 1, row, (uint32_t)step, (uint32_t)(step >> 32)), key);
+#pragma unroll
+          for (int e8 = 0; e8 < 8; ++e8) {
+            const int e = 8 * h + e8;
+            const uint4 bq = e8 < 4 ? p0 : p1;
+            const uint32_t x = (e & 3) == 0 ? bq.x : (e & 3) == 1 ? bq.y : (e & 3) == 2 ? bq.z : bq.w;
+            const float v = RVT::element_at(w, e);
+            if (v >= lo2 && v < M && (((x >> 9) << 1) | 1u) >= thr_i) {
+              const float z = __fdiv_rn(v, T);
+              const float need = s_lb - z - 1e-3f;
+              const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
+              const float u = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
+              if (u >= thr) atomicMax(&sh.best, argmax_key(z + gumbel_of_word(x), j0 + e));
+            }
+          }
+        }
+      } else {
+        uint32_t mm = RVT::ge_mask(w, lo2);
+#pragma unroll 1
+        while (mm) {
+          const int e = __ffs(mm) - 1;
+          mm &= mm - 1u;
+          const float v = RVT::element(w, e);
+          if (v < M) test(v, rv.index(g, e));
+        }
+      }
+      g = gn;
+      if (kAhead) {
+#pragma unroll
+        for (int q = 0; q < RVT::kWords; ++q) w[q] = wn[q];
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Bin weights of one select level.  A bin holds a count (top-k), the exact
+// fixed-point mass of its entries as a (lo, hi) pair (top-p, bins spanning
+// several keys) or, when every bin is a single key, a count that is scaled
+// here by that key's weight: the same fixed-point mass, since every entry of
+// the bin has the same value.
+enum BinMode { BIN_COUNT = 0, BIN_MASS = 1, BIN_KEY_COUNT = 2 };
+
+template <typename TIn>
+struct BinWeight {
+  const Shared* sh;
+  int mode;
+  uint32_t klo;  // key of bin 0 (BIN_KEY_COUNT)
+  float c, R;
+  __device__ __forceinline__ unsigned long long operator()(int b) const {
+    if (mode == BIN_MASS) return read_mass(&sh->hist[2 * b]);
+    const unsigned int n = sh->hist[b];
+    if (mode == BIN_COUNT || n == 0u) return n;
+    return (unsigned long long)n * mass_fixed(ex2(fmaf(KeyOps<TIn>::value(klo + (uint32_t)b), c, -R)));
+  }
+};
+
+// Find the highest bin b with above + (weight of bins >= b) >= target.
+// Thread t holds bins nb-1-4t .. nb-4-4t; one block scan over the threads.
+// With joint_p >= 0 the target becomes joint_p * (total weight of the level)
+// (written back to `target`, the same in every thread).
+// Writes sh.cut_bin (-1 when the total never reaches the target, possible
+// only through rounding of a top-p target), sh.cut_above (weight strictly
+// above bin b, including `above`) and sh.cut_mass (weight of bin b); returns
+// the level's total weight.  Two block barriers.
+template <typename W>
+__device__ __forceinline__ unsigned long long find_cut_bin(Shared& sh, int nb, unsigned long long above,
+                                                           unsigned long long& target, float joint_p,
+                                                           const W& weight) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int top = nb - 1 - t * kBinsPerThread;
+  unsigned long long w[kBinsPerThread], local = 0;
+#pragma unroll
+  for (int q = 0; q < kBinsPerThread; ++q) {
+    w[q] = top - q >= 0 ? weight(top - q) : 0ull;
+    local += w[q];
+  }
+  unsigned long long incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (t == 0) sh.cut_bin = -1;
+  if (lane == 31) sh.red_u64[warp] = incl;
+  __syncthreads();
+  unsigned long long base = 0, total = 0;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) {
+    const unsigned long long x = sh.red_u64[i];
+    base += i < warp ? x : 0ull;
+    total += x;
+  }
+  if (joint_p >= 0.f) target = __float2ull_ru(joint_p * __ull2float_rn(total));
+  if (target < 1ull) target = 1ull;
+  unsigned long long cum = above + base + incl - local;
+  if (cum < target && cum + local >= target) {
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+      if (cum + w[q] >= target) {
+        sh.cut_bin = top - q;
+        sh.cut_above = cum;
+        sh.cut_mass = w[q];
+        break;
+      }
+      cum += w[q];
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+struct SelResult {
+  uint32_t key;                 // kept set: entries with key >= this
+  unsigned long long mass_ge;   // weight of the kept entries
+};
+
+// Exact threshold select over the row entries with keys in [klo, khi], given
+// the weight `above` of the entries with larger keys: returns the largest key
+// kappa such that above + (weight of entries with key in [kappa, khi]) >=
+// target, where weight is 1 (top-k, target = k) or the fixed-point
+// probability mass exp((l - M)/T) * 2^40 (top-p, `mass`).  With joint_p >= 0
+// the target is joint_p * (total weight of the range).  Each level splits the
+// remaining key range into at most 2048 bins: bf16 keys (16 bits) need at most
+// two levels, fp32 keys at most three.  With `built` the first level's
+// histogram (same binning) is already in shared memory.  If the total weight
+// never reaches the target (possible only through rounding of a top-p target)
+// the whole range is kept.
+template <typename TIn>
+__device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo, uint32_t khi,
+                                  unsigned long long target, float joint_p, float R, float c,
+                                  unsigned long long above, bool mass, bool built) {
+  using K = KeyOps<TIn>;
+  unsigned long long mass_at = 0;
+  for (;;) {
+    const uint32_t width = khi - klo;
+    const int bits = width ? 32 - __clz(width) : 0;
+    const int shift = bits > kBinBits ? bits - kBinBits : 0;
+    const int nb = (int)(width >> shift) + 1;
+    const int mode = !mass ? BIN_COUNT : shift == 0 ? BIN_KEY_COUNT : BIN_MASS;
+    if (!built) {
+      for (int b = threadIdx.x; b < (mode == BIN_MASS ? 2 * nb : nb); b += kThreads) sh.hist[b] = 0u;
+      __syncthreads();
+      const float lo = K::value(klo), hi = K::value(khi);
+      const uint32_t base = klo, top = khi;
+      cs.each(lo, [&](float v, int64_t) {
+        const uint32_t kk = K::key(v);
+        if (v <= hi && kk >= base && kk <= top) {
+          const int bin = (int)((kk - base) >> shift);
+          if (mode == BIN_MASS)
+            add_mass(&sh.hist[2 * bin], mass_fixed(ex2(fmaf(v, c, -R))));
+          else
+            atomicAdd(&sh.hist[bin], 1u);
+        }
+      });
+      __syncthreads();
+    }
+    built = false;
+    const unsigned long long total =
+        find_cut_bin(sh, nb, above, target, joint_p, BinWeight<TIn>{&sh, mode, klo, c, R});
+    joint_p = -1.f;
+    const int b = sh.cut_bin;
+    if (b < 0) return SelResult{klo, above + total};  // only reachable on the first level
+    above = sh.cut_above;
+    mass_at = sh.cut_mass;
+    const uint32_t nlo = klo + ((uint32_t)b << shift);
+    const unsigned long long nhi = (unsigned long long)nlo + ((1ull << shift) - 1ull);
+    khi = nhi < (unsigned long long)khi ? (uint32_t)nhi : khi;
+    klo = nlo;
+    if (klo >= khi) break;  // a single key left
+    __syncthreads();        // the cut fields and the histogram are rewritten by the next level
+  }
+  return SelResult{klo, above + mass_at};
+}
+
+__device__ __forceinline__ void row_error(const KernelArgs& a, int64_t i, int mode, int err) {
+  if (threadIdx.x == 0) {
+    if (mode == MODE_SAMPLE) a.out_ids[i] = -1;
+    if (a.error_word) atomicOr(a.error_word, err);
+  }
+  if (mode == MODE_LOGPROBS) {
+    float* out = a.out_lp + i * a.vocab;
+    const float nan = __uint_as_float(0x7FC00000u);
+    for (int64_t j = threadIdx.x; j < a.vocab; j += kThreads) out[j] = nan;
+  }
+}
+
+// Write out[j] = kept(v_j) ? value(v_j) : -inf over the whole row, with
+// 16-byte stores to the output where its alignment allows.
+template <typename TIn, typename KeptF, typename ValF>
+__device__ __forceinline__ void write_row(const RowView<TIn>& rv, float* out, KeptF kept, ValF val) {
+  const int64_t V = rv.V;
+  const uintptr_t oa = reinterpret_cast<uintptr_t>(out);
+  int64_t head = (int64_t)(((16u - (oa & 15u)) & 15u) / 4u);
+  if ((oa & 3u) != 0u) head = V;  // not even float aligned: all scalar
+  if (head > V) head = V;
+  for (int64_t j = threadIdx.x; j < head; j += kThreads) {
+    const float v = rv.at(j);
+    out[j] = kept(v) ? val(v) : kNegInf;
+  }
+  const int64_t nq = (V - head) / 4;
+  for (int64_t q = threadIdx.x; q < nq; q += kThreads) {
+    const int64_t j = head + 4 * q;
+    float4 o;
+    float v0 = rv.at(j), v1 = rv.at(j + 1), v2 = rv.at(j + 2), v3 = rv.at(j + 3);
+    o.x = kept(v0) ? val(v0) : kNegInf;
+    o.y = kept(v1) ? val(v1) : kNegInf;
+    o.z = kept(v2) ? val(v2) : kNegInf;
+    o.w = kept(v3) ? val(v3) : kNegInf;
+    *reinterpret_cast<float4*>(out + j) = o;
+  }
+  for (int64_t j = head + 4 * nq + threadIdx.x; j < V; j += kThreads) {
+    const float v = rv.at(j);
+    out[j] = kept(v) ? val(v) : kNegInf;
+  }
+}
+
+template <typename TIn, int ROUTE, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelArgs a) {
+  using K = KeyOps<TIn>;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  float* gmax = reinterpret_cast<float*>(smem_raw + sizeof(Shared));
+  const int tid = threadIdx.x;
+  const int64_t ng_cap = group_slots(a.vocab);
+  float* cand_v = gmax + ng_cap;
+  int32_t* cand_j = reinterpret_cast<int32_t*>(cand_v + a.cand_cap);
+  const int64_t i = blockIdx.x;
+
+  // ---- row -> (logits row, request) ------------------------------------
+  int err = 0;
+  int64_t src = i;
+  if (a.gather) {
+    src = a.gather[i];
+    if (src < 0 || src >= a.logits_rows) err |= LS_ROW_ERR_BAD_GATHER;
+  }
+  int64_t req = i;
+  if (a.map_mode == MAP_T2R) {
+    req = a.t2r[i];
+  } else if (a.map_mode == MAP_SPEC) {
+    req = i < a.spec_decode_rows ? i / a.spec_per_req : a.spec_num_decode + (i - a.spec_decode_rows);
+  }
+  if (a.out_t2r && tid == 0) a.out_t2r[i] = (int32_t)req;
+  if (req < 0 || req >= a.num_requests) err |= LS_ROW_ERR_BAD_REQUEST;
+  if (err) {
+    row_error(a, i, MODE, err);
+    return;
+  }
+
+  const int64_t V = a.vocab;
+  RowView<TIn> rv;
+  rv.init(a.logits, src, a.stride, V);
+
+  // ---- streaming pass: group maxima, running max, online mass ----------
+  // Weights are 2^(v c - R) with c = log2(e) / T and R = RN(max * c): every
+  // mass in the row (total, candidate and kept masses) uses this one formula,
+  // so the rounding of R cancels in each ratio the cuts compare.  Each thread
+  // keeps its own reference r = RN(m c) for its running maximum m.
+  // Two register stages: the loads of the next groups are in flight while
+  // the current ones are reduced.  The first two stages are issued before
+  // the request's parameters are read.
+  using RV = RowView<TIn>;
+  constexpr int U = RV::kBytes == 2 ? 2 : 1;  // groups per stage
+  constexpr int STEP = U * kThreads;
+  auto issue = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (rv.full(g0 + u * kThreads)) rv.load_words(g0 + u * kThreads, w[u]);
+  };
+  uint32_t wa[U][RV::kWords], wb[U][RV::kWords];
+  issue(tid, wa);
+  issue(tid + STEP, wb);
+
+  const float T = a.temperature[req];
+  const int32_t k = a.top_k[req];
+  const float p = a.top_p[req];
+  const bool greedy = !(T >= 1e-5f);
+  const bool k_on = !greedy && (ROUTE & ROUTE_K) && k >= 1 && (int64_t)k < V;
+  const bool p_on = !greedy && (ROUTE & ROUTE_P) && p < 0.99999f;
+  const bool need_sum = !greedy && !k_on && (p_on || MODE == MODE_LOGPROBS);
+  const float c = greedy ? 0.f : kLog2e / T;
+
+  float m = kNegInf, r = 0.f;
+  f32x2 acc = 0ull;
+  const f32x2 c2 = pack2(c, c);
+  auto consume = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + u * kThreads;
+      if (g < rv.NG) {
+        if (!rv.full(g)) rv.load_words_partial(g, w[u]);
+        const float gm = RV::group_max(w[u]);
+        gmax[g] = gm;
+        if (need_sum) {
+          if (gm > m) {
+            const float rn = __fmul_rn(gm, c);  // rounded: never fused into r - rn
+            const float sc = ex2(r - rn);
+            acc = m > kNegInf ? mul2(acc, pack2(sc, sc)) : 0ull;
+            m = gm;
+            r = rn;
+          }
+          if (gm > kNegInf) acc = add2(acc, RV::exp_sum(w[u], c2, pack2(-r, -r)));
+        } else {
+          m = fmaxf(m, gm);
+        }
+      }
+    }
+  };
+  for (int g0 = tid; g0 < rv.NG; g0 += 2 * STEP) {
+    consume(g0, wa);
+    issue(g0 + 2 * STEP, wa);
+    consume(g0 + STEP, wb);
+    issue(g0 + 3 * STEP, wb);
+  }
+  // ---- one block reduction: row maximum, total mass, top-k bound --------
+  const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;  // its latency overlaps the reduction
+  // Each warp reduces its maximum, rescales every lane's sum to the warp's
+  // reference RN(max * c) and adds; after one barrier every warp combines the
+  // 16 warp results the same way (fixed order, so S is deterministic and the
+  // same in every warp).  For a top-k row each warp also extracts the j-th
+  // largest of its 32 thread maxima, j = ceil(k / 16): all 16 warps then hold
+  // >= j thread maxima (hence >= k distinct entries) at or above the smallest
+  // of those, gamma.
+  {
+    uint4* h4 = reinterpret_cast<uint4*>(sh.hist);
+    for (int q = tid; q < 2 * kBins / 4; q += kThreads) h4[q] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int lane = tid & 31;
+  {
+    const float mw = warp_max(m);
+    float sw = 0.f;
+    if (need_sum && mw > kNegInf) {
+      float lo, hi;
+      unpack2(acc, lo, hi);
+      sw = m > kNegInf ? (lo + hi) * ex2(r - __fmul_rn(mw, c)) : 0.f;
+      sw = warp_reduce(sw, OpAddF());
+    }
+    float gj = kNegInf;
+    if (k_on && k <= 32 * kWarps) {
+      const int jrank = (k + kWarps - 1) / kWarps;
+      float cur = m;
+      for (int t = 0; t < jrank; ++t) {
+        gj = warp_max(cur);
+        const unsigned holders = __ballot_sync(0xFFFFFFFFu, cur == gj);
+        if (lane == __ffs(holders) - 1) cur = kNegInf;
+      }
+    }
+    if (lane == 0) {
+      sh.red_m[tid >> 5] = mw;
+      sh.red_s[tid >> 5] = sw;
+      sh.red_f[tid >> 5] = gj;
+    }
+  }
+  if (tid == 0) {
+    sh.best = 0ull;
+    sh.acc[0] = 0u;
+    sh.acc[1] = 0u;
+    sh.min_index = 0x7FFFFFFF;
+    sh.cand_count = 0;
+    sh.tie_count = 0;
+  }
+  __syncthreads();
+  const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
+  const float M = warp_max(mq);
+  const float gamma = warp_min(lane < kWarps ? sh.red_f[lane] : kPosInf);
+  if (M == kNegInf) {
+    row_error(a, i, MODE, LS_ROW_ERR_NO_FINITE);
+    return;
+  }
+  const float R = __fmul_rn(M, c);  // reference exponent of the row (rounded product, never fused)
+  float S = 0.f;
+  if (need_sum && M < kPosInf) {
+    const float sq = lane < kWarps && mq > kNegInf ? sh.red_s[lane] * ex2(__fmul_rn(mq, c) - R) : 0.f;
+    S = warp_reduce(sq, OpAddF());
+  }
+  const bool tie_only = greedy || M == kPosInf;  // no temperature-scaled distribution
+
+  // ---- total mass when a NaN entry poisoned the online sum ---------------
+  if (!tie_only && need_sum && !(S <= FLT_MAX)) {
+    float nacc = 0.f;
+    for (int g = tid; g < rv.NG; g += kThreads) {
+      float v[kGroup];
+      rv.load(g, v);
+#pragma unroll
+      for (int q = 0; q < kGroup; ++q) {
+        const float x = v[q] == v[q] ? v[q] : kNegInf;
+        nacc += ex2(fmaf(x, c, -R));
+      }
+    }
+    S = block_reduce(nacc, OpAddF(), sh.red_f);
+  }
+
+  // ---- candidate bound --------------------------------------------------
+  // Every entry that a later phase needs is >= lc:
+  //  * ties-only rows (greedy, +inf maximum): the maximum itself;
+  //  * top-k: gamma (at least k entries are >= gamma);
+  //  * top-p alone: the entries below Lp carry less than (1 - p) S e^-2, so
+  //    the cut lies above Lp;
+  //  * no filter: an entry with z more than the noise span below max z can
+  //    never beat the maximum's perturbed score.
+  const float lg = M - kGumbelSpan * T;
+  float lc;
+  int kind = 0;  // first-level histogram: 0 none, 1 count (top-k), 2 mass (top-p alone)
+  if (tie_only) {
+    lc = M;
+  } else if (k_on) {
+    lc = gamma > kNegInf ? gamma : -FLT_MAX;
+    kind = 1;
+  } else if (p_on) {
+    const float Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
+    lc = fminf(fmaxf(Lp, -FLT_MAX), M);
+    kind = 2;
+  } else {
+    // Unfiltered rows build no list: sampling reads only the groups above its
+    // noise bounds (the maximum's ties, then the pruned Gumbel pass) straight
+    // from global memory, and unfiltered log-probs need no candidates at all.
+    lc = kPosInf;
+  }
+  lc = fmaxf(lc, -FLT_MAX);
+  const uint32_t key_max = K::key(M);
+  const uint32_t klo1 = K::key(lc);
+  const uint32_t width1 = key_max - klo1;
+  const int bits1 = width1 ? 32 - __clz(width1) : 0;
+  const int shift1 = bits1 > kBinBits ? bits1 - kBinBits : 0;
+  // first select level, built while collecting (the binning radix_select uses)
+  const int mode1 = kind == 1 ? BIN_COUNT : shift1 == 0 ? BIN_KEY_COUNT : BIN_MASS;
+  // sampling rows score the maximum's ties while collecting
+  const bool ties_in_take = MODE == MODE_SAMPLE && !tie_only;
+
+  // ---- collect: candidate groups -> entries >= lc -----------------------
+  // Each warp scans chunks of 128 group maxima (four per lane, one 16-byte
+  // shared load), chunk q going to warp q mod 16, and lists its candidate
+  // groups (maximum >= lc) in its own slice of the group list.  When the
+  // slice could overflow, and at the end, the warp loads the listed groups
+  // (two per lane per round, all loads in flight at once) and takes their
+  // entries >= lc: they are appended to the shared-memory candidate list (one
+  // atomic per warp and round), feed the first select level's histogram and,
+  // when sampling, the maximum's ties are recorded.  No block barrier until
+  // every warp is done.
+  using RVT = RowView<TIn>;
+  int count = 0;
+  // Entry >= lc of a loaded group: append it to the list and feed the first
+  // select level's histogram.
+  auto take = [&](int g, const uint32_t (&w)[RVT::kWords], uint32_t mm, int at) {
+#pragma unroll 1
+    while (mm) {
+      const int e = __ffs(mm) - 1;
+      mm &= mm - 1u;
+      const float x = RVT::element(w, e);
+      if (at < a.cand_cap) {
+        cand_v[at] = x;
+        cand_j[at] = (int32_t)rv.index(g, e);
+      }
+      ++at;
+      if (kind != 0) {
+        const uint32_t kk = K::key(x);
+        if (kk >= klo1 && kk <= key_max) {
+          const int bin = (int)((kk - klo1) >> shift1);
+          if (mode1 == BIN_MASS)
+            add_mass(&sh.hist[2 * bin], mass_fixed(ex2(fmaf(x, c, -R))));
+          else
+            atomicAdd(&sh.hist[bin], 1u);
+        }
+      }
+      if (ties_in_take && x >= M) {
+        const int q = atomicAdd(&sh.tie_count, 1);
+        if (q < kTieList) sh.tie_j[q] = (int)rv.index(g, e);
+      }
+    }
+  };
+  if (lc <= M) {
+    int* wl = sh.glist + (tid >> 5) * kWarpList;
+    // load the n listed groups of this warp (kPer per lane per round, all
+    // loads in flight at once) and take their entries
+    constexpr int kPer = RVT::kWords <= 8 ? 2 : 1;
+    auto flush = [&](int n) {
+      __syncwarp();
+      for (int c0 = 0; c0 < n; c0 += 32 * kPer) {
+        uint32_t w[kPer][RVT::kWords];
+        int gg[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int cu = c0 + 32 * u + lane;
+          gg[u] = cu < n ? wl[cu] : -1;
+          if (gg[u] >= 0 && rv.full(gg[u])) rv.load_words(gg[u], w[u]);
+        }
+        uint32_t mm[kPer];
+        int cnt = 0;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          mm[u] = 0u;
+          if (gg[u] >= 0) {
+            if (!rv.full(gg[u])) rv.load_words_partial(gg[u], w[u]);
+            mm[u] = RVT::ge_mask(w[u], lc);
+            cnt += __popc(mm[u]);
+          }
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t2;
+        }
+        int base = 0;
+        if (lane == 31) base = atomicAdd(&sh.cand_count, incl);
+        int at = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          if (mm[u]) take(gg[u], w[u], mm[u], at);
+          at += __popc(mm[u]);
+        }
+      }
+      __syncwarp();
+    };
+    // Each thread tests the maxima of its own groups (tid + 512 s, the ones
+    // it streamed), 32 slots at a time; one warp prefix over the per-thread
+    // counts places the candidate groups in the warp's list slice, which is
+    // loaded and taken kWarpList groups at a time.
+    const int nslots = (rv.NG + kThreads - 1) / kThreads;
+    for (int sb = 0; sb < nslots; sb += 32) {
+      const int send = min(32, nslots - sb);
+      uint32_t mask = 0u;
+#pragma unroll 8
+      for (int q = 0; q < send; ++q) {
+        const int g = tid + (sb + q) * kThreads;
+        if (g < rv.NG && gmax[g] >= lc) mask |= 1u << q;
+      }
+      const int cnt = __popc(mask);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t2 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t2;
+      }
+      const int wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      for (int w0 = 0; w0 < wtot; w0 += kWarpList) {
+        uint32_t mm = mask;
+        int at = incl - cnt;
+        while (mm) {
+          const int q = __ffs(mm) - 1;
+          mm &= mm - 1u;
+          if (at >= w0 && at < w0 + kWarpList) wl[at - w0] = tid + (sb + q) * kThreads;
+          ++at;
+        }
+        flush(min(kWarpList, wtot - w0));
+      }
+    }
+    __syncthreads();
+    count = sh.cand_count;
+  }
+  const Cands<TIn> cs{&rv, gmax, cand_v, cand_j, count, lc <= M && count <= a.cand_cap};
+
+  // The maximum's ties: lowest index (greedy), count (log-probs of ties-only
+  // rows) or exact Gumbel score (sampling; the best is a lower bound of the
+  // winner's score).  Sampling rows that collected candidates recorded their
+  // ties there: one thread scores each (sh.best is next read after the cut's
+  // barriers); only more than kTieList ties take a pass over the list.
+  const int nties = ties_in_take && lc <= M ? sh.tie_count : -1;
+  if (nties >= 0 && nties <= kTieList) {
+    if (tid < nties) score_entry(&sh.best, M, T, seed, a.step, (uint32_t)i, sh.tie_j[tid]);
+  } else if (tie_only || MODE == MODE_SAMPLE) {
+    cs.each(M, [&](float x, int64_t j) {
+      if (MODE == MODE_LOGPROBS) {
+        atomicAdd(&sh.acc[0], 1u);
+      } else if (greedy) {
+        atomicMin(&sh.min_index, (int)j);
+      } else {
+        const float z = M == kPosInf ? 0.f : __fdiv_rn(x, T);
+        atomicMax(&sh.best, argmax_key(z + gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j)), j));
+      }
+    });
+    __syncthreads();
+  }
+  if (tie_only) {
+    if (MODE == MODE_SAMPLE) {
+      if (tid == 0) a.out_ids[i] = greedy ? sh.min_index : argmax_index(sh.best);
+    } else {
+      const float lp = -logf((float)sh.acc[0]);
+      write_row(rv, a.out_lp + i * V, [&](float v) { return v >= M; }, [&](float) { return lp; });
+    }
+    return;
+  }
+
+  // ---- exact top-k and top-p cuts ---------------------------------------
+  uint32_t lo_key = K::key(-FLT_MAX);  // no filter: every finite entry
+  unsigned long long kept_mass = 0ull;
+  if (kind != 0) {
+    // the first level's histogram was built while collecting
+    const unsigned long long target =
+        kind == 1 ? (unsigned long long)k : max(1ull, __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale));
+    const SelResult r1 = radix_select<TIn>(sh, cs, klo1, key_max, target, -1.f, R, c, 0ull, kind == 2, true);
+    lo_key = r1.key;
+    kept_mass = r1.mass_ge;
+  }
+  if (k_on && p_on) {
+    const SelResult r2 =
+        radix_select<TIn>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), R, c, 0ull, true, false);
+    lo_key = r2.key;
+    kept_mass = r2.mass_ge;
+  }
+  const float lo_val = K::value(lo_key);
+
+  if (MODE == MODE_SAMPLE) {
+    // ---- Gumbel-max over the kept set ------------------------------------
+    gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, seed, a.step, (uint32_t)i);
+    if (tid == 0) a.out_ids[i] = argmax_index(sh.best);
+  } else {
+    // ---- log-probs of the processed distribution -------------------------
+    float lnS;
+    if (p_on) {
+      lnS = logf(__ull2float_rn(kept_mass) / kMassScale);
+    } else if (k_on) {
+      cs.each(lo_val, [&](float v, int64_t) { add_mass(sh.acc, mass_fixed(ex2(fmaf(v, c, -R)))); });
+      __syncthreads();
+      lnS = logf(__ull2float_rn(read_mass(sh.acc)) / kMassScale);
+    } else {
+      lnS = logf(S);
+    }
+    // The masses are 2^(v c - R) = exp((v - M) / T) * 2^(M c - R); remove the
+    // exactly computable residual of R's rounding from the normaliser.
+    lnS -= fmaf(M, c, -R) * 0.6931471805599453f;
+    write_row(rv, a.out_lp + i * V, [&](float v) { return v >= lo_val; },
+              [&](float v) { return __fdiv_rn(v - M, T) - lnS; });
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+// Shared memory of one CTA: fixed part, group maxima (worst-case row
+// alignment), candidate list of `cap` (value, index) pairs.
+static size_t smem_bytes(int64_t vocab, int cap) {
+  const int64_t ng = group_slots(vocab);
+  return sizeof(Shared) + (size_t)ng * sizeof(float) + (size_t)cap * (sizeof(float) + sizeof(int32_t));
+}
+
+// Candidate-list capacity: up to 8192 entries while a CTA stays within 96 KB
+// of shared memory, never below 256.  Two such CTAs per SM leave at least
+// 60 KB of the SM's 256 KB L1/shared array to L1, which the streaming loads
+// need for their requests in flight: with 104 KB per CTA a plain 256-row
+// bf16 read of this shape was measured a quarter slower.
+static int cand_capacity(int64_t vocab) {
+  constexpr size_t kPerCta = 96 * 1024;
+  const size_t base = smem_bytes(vocab, 0);
+  int cap = 8192;
+  while (cap > 256 && base + (size_t)cap * 8 > kPerCta) cap -= 256;
+  return cap;
+}
+
+constexpr int kMaxDevices = 64;
+
+static int max_dyn_smem() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices && (v = cache[dev].load(std::memory_order_relaxed)) > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+template <typename TIn, int ROUTE, int MODE>
+static ls_status launch_rows(const KernelArgs& a, int32_t n, size_t smem, cudaStream_t stream) {
+  auto kern = sampler_row_kernel<TIn, ROUTE, MODE>;
+  // The dynamic shared-memory opt-in is set once per device and size class.
+  static std::atomic<size_t> opted[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LS_ERR_CUDA;
+  if (smem > 48 * 1024 && (dev < 0 || dev >= kMaxDevices || opted[dev].load(std::memory_order_relaxed) < smem)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return LS_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) opted[dev].store(smem, std::memory_order_relaxed);
+  }
+  kern<<<dim3((unsigned)n), dim3(kThreads), smem, stream>>>(a);
+  return cudaPeekAtLastError() == cudaSuccess ? LS_OK : LS_ERR_CUDA;
+}
+
+template <int MODE>
+ls_status dispatch(KernelArgs a, ls_dtype dtype, int route, int32_t n, cudaStream_t stream) {
+  a.cand_cap = cand_capacity(a.vocab);
+  const size_t smem = smem_bytes(a.vocab, a.cand_cap);
+  const int lim = max_dyn_smem();
+  if (lim <= 0) return LS_ERR_CUDA;
+  if (smem > (size_t)lim) return LS_ERR_UNSUPPORTED;
+  if (dtype == LS_DTYPE_BF16) {
+    switch (route) {
+      case ROUTE_NONE: return launch_rows<bf16_tag, ROUTE_NONE, MODE>(a, n, smem, stream);
+      case ROUTE_K: return launch_rows<bf16_tag, ROUTE_K, MODE>(a, n, smem, stream);
+      case ROUTE_P: return launch_rows<bf16_tag, ROUTE_P, MODE>(a, n, smem, stream);
+      default: return launch_rows<bf16_tag, ROUTE_KP, MODE>(a, n, smem, stream);
+    }
+  }
+  switch (route) {
+    case ROUTE_NONE: return launch_rows<float, ROUTE_NONE, MODE>(a, n, smem, stream);
+    case ROUTE_K: return launch_rows<float, ROUTE_K, MODE>(a, n, smem, stream);
+    case ROUTE_P: return launch_rows<float, ROUTE_P, MODE>(a, n, smem, stream);
+    default: return launch_rows<float, ROUTE_KP, MODE>(a, n, smem, stream);
+  }
+}
+
+static bool params_ok(const ls_params* prm, bool need_seed) {
+  return prm && prm->temperature && prm->top_k && prm->top_p && (!need_seed || prm->seed) && prm->num_requests >= 1;
+}
+
+static bool common_ok(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride) {
+  return logits && (dtype == LS_DTYPE_F32 || dtype == LS_DTYPE_BF16) && vocab >= 1 && row_stride >= vocab &&
+         logits_rows >= 1 && vocab <= 0x7FFFFFF0ll;
+}
+
+static KernelArgs make_args(const void* logits, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                            const int32_t* gather, const ls_params* prm, uint64_t step, int32_t* error_word) {
+  KernelArgs a{};
+  a.logits = logits;
+  a.logits_rows = logits_rows;
+  a.vocab = vocab;
+  a.stride = row_stride;
+  a.gather = gather;
+  a.temperature = prm->temperature;
+  a.top_k = prm->top_k;
+  a.top_p = prm->top_p;
+  a.seed = prm->seed;
+  a.num_requests = prm->num_requests;
+  a.step = step;
+  a.error_word = error_word;
+  return a;
+}
+
+}  // namespace lsg
