@@ -149,6 +149,37 @@ ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, 
                        int32_t num_rows, const int32_t* gather_indices, const int32_t* token_to_request_index,
                        const ls_params* params, float* out_log_probs, int32_t* error_word, void* stream);
 
+/*
+ * ls_sample_log_probs -- sample n token ids and, from the same single read of
+ * the logits, their log-probs.
+ *
+ * Follows "core.inference.sampling.flashinfer_sampling" (FlashInferSampling.
+ * sample_kernel and log_probs_kernel) and the TokenSpeed "backends/triton.py"
+ * page (TritonSamplingBackend.sample followed by _write_logprob_outputs,
+ * which fills next_token_logprobs with selected_token_logprobs(logits,
+ * sampled)): what ls_sample followed by ls_log_probs and a selected-token
+ * log-prob would compute, with the logits read from HBM once instead of
+ * twice.
+ *
+ *   out_ids                device int32[n]: exactly the ids ls_sample returns
+ *                          for the same arguments
+ *   out_log_probs          device float[n * vocab] or NULL: log-probs of the
+ *                          processed distribution, as ls_log_probs writes them
+ *                          (the route flags switch filters off as for ls_sample)
+ *   out_selected_log_probs device float[n] or NULL: log-probability of the
+ *                          sampled id under the raw logits (no temperature, no
+ *                          filter): l_id - ln sum_j exp(l_j) over the row, NaN
+ *                          logits read as -inf; a row whose maximum is +inf
+ *                          gives -ln(#(+inf entries)) for a +inf id
+ * With both optional outputs NULL the call is ls_sample.  Error rows: id -1,
+ * NaN log-probs.  Other arguments as for ls_sample.
+ */
+ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
+                              int64_t row_stride, int32_t n, const int32_t* gather_indices,
+                              const int32_t* token_to_request_index, const ls_params* params, uint64_t step,
+                              int no_top_k, int no_top_p, int32_t* out_ids, float* out_log_probs,
+                              float* out_selected_log_probs, int32_t* error_word, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* ls_status_string(ls_status s);
 

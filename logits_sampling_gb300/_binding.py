@@ -46,6 +46,8 @@ def load_library():
     lib.ls_sample_speculative.restype = ci
     lib.ls_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, P, P]
     lib.ls_log_probs.restype = ci
+    lib.ls_sample_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P, P, P]
+    lib.ls_sample_log_probs.restype = ci
     lib.ls_status_string.argtypes = [ci]
     lib.ls_status_string.restype = ctypes.c_char_p
     lib.ls_max_vocab.argtypes = [ci]
@@ -201,3 +203,37 @@ def log_probs(logits, params, num_rows=None, gather_indices=None, token_to_reque
     if st != LS_OK:
         raise LSError(st, "ls_log_probs")
     return out
+
+
+def sample_log_probs(logits, n, params, step, no_top_k, no_top_p, gather_indices=None, token_to_request_index=None,
+                     want_log_probs=True, want_selected=True, out=None, out_log_probs=None, out_selected=None,
+                     error_word=None, stream=None):
+    """ls_sample_log_probs: returns (ids int32 [n], log_probs float32 [n, vocab] or None,
+    selected float32 [n] or None) from one read of the logits."""
+    import torch
+    lib = load_library()
+    ptr, dt, rows, V, stride = _logits_desc(logits)
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=logits.device)
+    if want_log_probs and out_log_probs is None:
+        out_log_probs = torch.empty((n, V), dtype=torch.float32, device=logits.device)
+    if want_selected and out_selected is None:
+        out_selected = torch.empty(n, dtype=torch.float32, device=logits.device)
+    if not want_log_probs:
+        out_log_probs = None
+    if not want_selected:
+        out_selected = None
+    if out_log_probs is not None and (out_log_probs.dtype != torch.float32 or not out_log_probs.is_contiguous()
+                                      or out_log_probs.numel() < n * V):
+        raise ValueError("out_log_probs must be a contiguous float32 tensor of n * vocab entries")
+    if out_selected is not None and (out_selected.dtype != torch.float32 or out_selected.numel() < n):
+        raise ValueError("out_selected must be a float32 tensor of n entries")
+    prm = params.as_struct()
+    st = lib.ls_sample_log_probs(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
+                                 _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
+                                 int(step), int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"),
+                                 _dptr(out_log_probs), _dptr(out_selected), _i32(error_word, "error_word"),
+                                 _stream(stream))
+    if st != LS_OK:
+        raise LSError(st, "ls_sample_log_probs")
+    return out, out_log_probs, out_selected

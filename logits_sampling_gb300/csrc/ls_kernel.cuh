@@ -36,7 +36,9 @@
 namespace lsg {
 
 enum MapMode { MAP_IDENTITY = 0, MAP_T2R = 1, MAP_SPEC = 2 };
-enum Mode { MODE_SAMPLE = 0, MODE_LOGPROBS = 1 };
+// MODE_BOTH: ids, and from the same pass the processed log-prob rows and/or
+// the selected token's log-prob under the raw logits.
+enum Mode { MODE_SAMPLE = 0, MODE_LOGPROBS = 1, MODE_BOTH = 2 };
 enum Route { ROUTE_NONE = 0, ROUTE_K = 1, ROUTE_P = 2, ROUTE_KP = 3 };
 
 struct KernelArgs {
@@ -56,7 +58,8 @@ struct KernelArgs {
   uint64_t step;
   int32_t* out_ids;
   int32_t* out_t2r;
-  float* out_lp;
+  float* out_lp;   // log-prob rows (MODE_LOGPROBS; MODE_BOTH when not NULL)
+  float* out_sel;  // raw log-prob of the sampled id per row (MODE_BOTH, when not NULL)
   int32_t* error_word;
   int32_t cand_cap;  // capacity of the shared-memory candidate list
 };
@@ -91,6 +94,7 @@ struct alignas(16) Shared {
   int glist[kWarps * kWarpList];  // candidate group indices, one slice per warp
   float red_m[kWarps];
   float red_s[kWarps];
+  float red_s2[kWarps];  // raw (T = 1) mass per warp, for the selected log-prob
 };
 
 // Exact 64-bit add into a (lo, hi) pair of u32 counters with two native
@@ -366,6 +370,23 @@ __device__ __forceinline__ void visit_candidates(const RowView<TIn>& rv, const f
 // bound into a shared-memory list (value, index); all later phases then read
 // that list.  If the list would overflow, phases fall back to re-reading the
 // candidate groups from global memory.
+// Total mass 2^(v c - R) of a row with NaN entries (read as -inf): a second
+// pass over the row, off the common path.  All threads call it.
+template <typename TIn>
+__device__ float total_mass_nan(const RowView<TIn>& rv, float c, float R, float* red) {
+  float nacc = 0.f;
+  for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
+    float v[kGroup];
+    rv.load(g, v);
+#pragma unroll
+    for (int q = 0; q < kGroup; ++q) {
+      const float x = v[q] == v[q] ? v[q] : kNegInf;
+      nacc += ex2(fmaf(x, c, -R));
+    }
+  }
+  return block_reduce(nacc, OpAddF(), red);
+}
+
 template <typename TIn>
 struct Cands {
   const RowView<TIn>* rv;
@@ -666,10 +687,11 @@ __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo
 
 __device__ __forceinline__ void row_error(const KernelArgs& a, int64_t i, int mode, int err) {
   if (threadIdx.x == 0) {
-    if (mode == MODE_SAMPLE) a.out_ids[i] = -1;
+    if (mode != MODE_LOGPROBS) a.out_ids[i] = -1;
+    if (mode == MODE_BOTH && a.out_sel) a.out_sel[i] = __uint_as_float(0x7FC00000u);
     if (a.error_word) atomicOr(a.error_word, err);
   }
-  if (mode == MODE_LOGPROBS) {
+  if (mode == MODE_LOGPROBS || (mode == MODE_BOTH && a.out_lp)) {
     float* out = a.out_lp + i * a.vocab;
     const float nan = __uint_as_float(0x7FC00000u);
     for (int64_t j = threadIdx.x; j < a.vocab; j += kThreads) out[j] = nan;
@@ -768,12 +790,16 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   const bool greedy = !(T >= 1e-5f);
   const bool k_on = !greedy && (ROUTE & ROUTE_K) && k >= 1 && (int64_t)k < V;
   const bool p_on = !greedy && (ROUTE & ROUTE_P) && p < 0.99999f;
-  const bool need_sum = !greedy && !k_on && (p_on || MODE == MODE_LOGPROBS);
+  constexpr bool kSample = MODE != MODE_LOGPROBS;  // an id per row
+  const bool want_lp = MODE == MODE_LOGPROBS || (MODE == MODE_BOTH && a.out_lp != nullptr);
+  const bool want_raw = MODE == MODE_BOTH && a.out_sel != nullptr;  // raw log-sum-exp of the row
+  const bool need_sum = !greedy && !k_on && (p_on || want_lp);
   const float c = greedy ? 0.f : kLog2e / T;
 
-  float m = kNegInf, r = 0.f;
-  f32x2 acc = 0ull;
+  float m = kNegInf, r = 0.f, r2 = 0.f;
+  f32x2 acc = 0ull, acc2 = 0ull;
   const f32x2 c2 = pack2(c, c);
+  const f32x2 l2 = pack2(kLog2e, kLog2e);
   auto consume = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -782,6 +808,16 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
         if (!rv.full(g)) rv.load_words_partial(g, w[u]);
         const float gm = RV::group_max(w[u]);
         gmax[g] = gm;
+        if (MODE == MODE_BOTH && want_raw) {
+          // raw weights 2^(v log2 e - r2) beside the processed ones
+          if (gm > m) {
+            const float rn = __fmul_rn(gm, kLog2e);
+            const float sc = ex2(r2 - rn);
+            acc2 = m > kNegInf ? mul2(acc2, pack2(sc, sc)) : 0ull;
+            r2 = rn;
+          }
+          if (gm > kNegInf) acc2 = add2(acc2, RV::exp_sum(w[u], l2, pack2(-r2, -r2)));
+        }
         if (need_sum) {
           if (gm > m) {
             const float rn = __fmul_rn(gm, c);  // rounded: never fused into r - rn
@@ -804,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     issue(g0 + 3 * STEP, wb);
   }
   // ---- one block reduction: row maximum, total mass, top-k bound --------
-  const uint64_t seed = MODE == MODE_SAMPLE ? a.seed[req] : 0ull;  // its latency overlaps the reduction
+  const uint64_t seed = kSample ? a.seed[req] : 0ull;  // its latency overlaps the reduction
   // Each warp reduces its maximum, rescales every lane's sum to the warp's
   // reference RN(max * c) and adds; after one barrier every warp combines the
   // 16 warp results the same way (fixed order, so S is deterministic and the
@@ -826,6 +862,13 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       sw = m > kNegInf ? (lo + hi) * ex2(r - __fmul_rn(mw, c)) : 0.f;
       sw = warp_reduce(sw, OpAddF());
     }
+    float sw2 = 0.f;
+    if (MODE == MODE_BOTH && want_raw && mw > kNegInf) {
+      float lo, hi;
+      unpack2(acc2, lo, hi);
+      sw2 = m > kNegInf ? (lo + hi) * ex2(r2 - __fmul_rn(mw, kLog2e)) : 0.f;
+      sw2 = warp_reduce(sw2, OpAddF());
+    }
     float gj = kNegInf;
     if (k_on && k <= 32 * kWarps) {
       const int jrank = (k + kWarps - 1) / kWarps;
@@ -839,6 +882,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     if (lane == 0) {
       sh.red_m[tid >> 5] = mw;
       sh.red_s[tid >> 5] = sw;
+      sh.red_s2[tid >> 5] = sw2;
       sh.red_f[tid >> 5] = gj;
     }
   }
@@ -865,21 +909,17 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     S = warp_reduce(sq, OpAddF());
   }
   const bool tie_only = greedy || M == kPosInf;  // no temperature-scaled distribution
+  // raw mass S2 = sum 2^(v log2 e - R2), R2 = RN(M log2 e) (MODE_BOTH, selected log-prob)
+  const float R2 = __fmul_rn(M, kLog2e);
+  float S2 = 0.f;
+  if (MODE == MODE_BOTH && want_raw && M < kPosInf) {
+    const float sq = lane < kWarps && mq > kNegInf ? sh.red_s2[lane] * ex2(__fmul_rn(mq, kLog2e) - R2) : 0.f;
+    S2 = warp_reduce(sq, OpAddF());
+    if (!(S2 <= FLT_MAX)) S2 = total_mass_nan(rv, kLog2e, R2, sh.red_f);
+  }
 
   // ---- total mass when a NaN entry poisoned the online sum ---------------
-  if (!tie_only && need_sum && !(S <= FLT_MAX)) {
-    float nacc = 0.f;
-    for (int g = tid; g < rv.NG; g += kThreads) {
-      float v[kGroup];
-      rv.load(g, v);
-#pragma unroll
-      for (int q = 0; q < kGroup; ++q) {
-        const float x = v[q] == v[q] ? v[q] : kNegInf;
-        nacc += ex2(fmaf(x, c, -R));
-      }
-    }
-    S = block_reduce(nacc, OpAddF(), sh.red_f);
-  }
+  if (!tie_only && need_sum && !(S <= FLT_MAX)) S = total_mass_nan(rv, c, R, sh.red_f);
 
   // ---- candidate bound --------------------------------------------------
   // Every entry that a later phase needs is >= lc:
@@ -916,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // first select level, built while collecting (the binning radix_select uses)
   const int mode1 = kind == 1 ? BIN_COUNT : shift1 == 0 ? BIN_KEY_COUNT : BIN_MASS;
   // sampling rows score the maximum's ties while collecting
-  const bool ties_in_take = MODE == MODE_SAMPLE && !tie_only;
+  const bool ties_in_take = kSample && !tie_only;
 
   // ---- collect: candidate groups -> entries >= lc -----------------------
   // Each warp scans chunks of 128 group maxima (four per lane, one 16-byte
@@ -1049,23 +1089,35 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   const int nties = ties_in_take && lc <= M ? sh.tie_count : -1;
   if (nties >= 0 && nties <= kTieList) {
     if (tid < nties) score_entry(&sh.best, M, T, seed, a.step, (uint32_t)i, sh.tie_j[tid]);
-  } else if (tie_only || MODE == MODE_SAMPLE) {
+  } else if (tie_only || kSample) {
     cs.each(M, [&](float x, int64_t j) {
-      if (MODE == MODE_LOGPROBS) {
-        atomicAdd(&sh.acc[0], 1u);
-      } else if (greedy) {
-        atomicMin(&sh.min_index, (int)j);
-      } else {
-        const float z = M == kPosInf ? 0.f : __fdiv_rn(x, T);
-        atomicMax(&sh.best, argmax_key(z + gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j)), j));
+      if (MODE != MODE_SAMPLE && tie_only) atomicAdd(&sh.acc[0], 1u);
+      if (kSample) {
+        if (greedy) {
+          atomicMin(&sh.min_index, (int)j);
+        } else {
+          const float z = M == kPosInf ? 0.f : __fdiv_rn(x, T);
+          atomicMax(&sh.best, argmax_key(z + gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j)), j));
+        }
       }
     });
     __syncthreads();
   }
+  // Raw log-prob of the sampled entry: (v - M) - ln sum exp(v - M); the raw
+  // masses carry the residual 2^(M log2 e - R2) of R2's rounding.  A +inf
+  // maximum shares the probability among its +inf entries.
+  auto selected_lp = [&](int32_t id) {
+    const float v = rv.at(id);
+    if (M == kPosInf) return v == kPosInf ? -logf((float)sh.acc[0]) : kNegInf;
+    return (v - M) - (logf(S2) - fmaf(M, kLog2e, -R2) * 0.6931471805599453f);
+  };
   if (tie_only) {
-    if (MODE == MODE_SAMPLE) {
-      if (tid == 0) a.out_ids[i] = greedy ? sh.min_index : argmax_index(sh.best);
-    } else {
+    if (kSample && tid == 0) {
+      const int32_t id = greedy ? sh.min_index : argmax_index(sh.best);
+      a.out_ids[i] = id;
+      if (MODE == MODE_BOTH && want_raw) a.out_sel[i] = selected_lp(id);
+    }
+    if (want_lp) {
       const float lp = -logf((float)sh.acc[0]);
       write_row(rv, a.out_lp + i * V, [&](float v) { return v >= M; }, [&](float) { return lp; });
     }
@@ -1091,11 +1143,16 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   }
   const float lo_val = K::value(lo_key);
 
-  if (MODE == MODE_SAMPLE) {
+  if (kSample) {
     // ---- Gumbel-max over the kept set ------------------------------------
     gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, seed, a.step, (uint32_t)i);
-    if (tid == 0) a.out_ids[i] = argmax_index(sh.best);
-  } else {
+    if (tid == 0) {
+      const int32_t id = argmax_index(sh.best);
+      a.out_ids[i] = id;
+      if (MODE == MODE_BOTH && want_raw) a.out_sel[i] = selected_lp(id);
+    }
+  }
+  if (want_lp) {
     // ---- log-probs of the processed distribution -------------------------
     float lnS;
     if (p_on) {

@@ -7,6 +7,7 @@
 namespace lsg {
 extern template ls_status dispatch<MODE_SAMPLE>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
 extern template ls_status dispatch<MODE_LOGPROBS>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
+extern template ls_status dispatch<MODE_BOTH>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
 }  // namespace lsg
 
 using namespace lsg;
@@ -73,6 +74,29 @@ ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, 
   a.map_mode = token_to_request_index ? MAP_T2R : MAP_IDENTITY;
   a.out_lp = out_log_probs;
   return dispatch<MODE_LOGPROBS>(a, dtype, ROUTE_KP, num_rows, static_cast<cudaStream_t>(stream));
+}
+
+ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
+                              int64_t row_stride, int32_t n, const int32_t* gather_indices,
+                              const int32_t* token_to_request_index, const ls_params* params, uint64_t step,
+                              int no_top_k, int no_top_p, int32_t* out_ids, float* out_log_probs,
+                              float* out_selected_log_probs, int32_t* error_word, void* stream) {
+  if (n < 0) return LS_ERR_INVALID_ARG;
+  if (n == 0) return LS_OK;
+  if (!common_ok(logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, true) || !out_ids)
+    return LS_ERR_INVALID_ARG;
+  if (!gather_indices && (int64_t)n > logits_rows) return LS_ERR_INVALID_ARG;
+  if (!token_to_request_index && n > params->num_requests) return LS_ERR_INVALID_ARG;
+  KernelArgs a = make_args(logits, logits_rows, vocab, row_stride, gather_indices, params, step, error_word);
+  a.t2r = token_to_request_index;
+  a.map_mode = token_to_request_index ? MAP_T2R : MAP_IDENTITY;
+  a.out_ids = out_ids;
+  a.out_lp = out_log_probs;
+  a.out_sel = out_selected_log_probs;
+  const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
+  if (!out_log_probs && !out_selected_log_probs)  // ids only: the sampling kernels
+    return dispatch<MODE_SAMPLE>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
+  return dispatch<MODE_BOTH>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
 }
 
 const char* ls_status_string(ls_status s) {

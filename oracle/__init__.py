@@ -54,6 +54,8 @@ def _load():
         lib.oracle_log_probs.argtypes = [P, ctypes.c_int, i64, i64, i64, i32, P, P, P, P, P, i32, P, P, P, P,
                                          ctypes.c_int]
         lib.oracle_log_probs.restype = ctypes.c_int
+        lib.oracle_selected_log_probs.argtypes = [P, ctypes.c_int, i64, i64, i64, i32, P, P, P]
+        lib.oracle_selected_log_probs.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -165,3 +167,16 @@ def log_probs(logits, dtype, num_rows, temperature, top_k, top_p, gather_indices
     if rc != 0:
         raise RuntimeError(f"oracle_log_probs failed ({rc})")
     return {"lp": lp, "kept": kept.astype(bool), "flags": flags, "error_word": int(err[0])}
+
+
+def selected_log_probs(logits, dtype, ids, gather_indices=None, vocab=None):
+    """Reference log-probability of ids[i] under the raw logits of row i
+    (log-softmax of the row, no temperature or filter), float64 [n]."""
+    a = _logits_args(logits, dtype)
+    rows, stride = a.shape
+    V = stride if vocab is None else vocab
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    g = None if gather_indices is None else np.ascontiguousarray(gather_indices, dtype=np.int32)
+    out = np.zeros(len(ids), dtype=np.float64)
+    _load().oracle_selected_log_probs(_ptr(a), dtype, rows, V, stride, len(ids), _ptr(g), _ptr(ids), _ptr(out))
+    return out

@@ -35,6 +35,9 @@
  *   8. Log-probs of the processed distribution ("core.inference.sampling.
  *      flashinfer_sampling" page, log_probs_kernel): z - max_K z -
  *      ln sum_K exp(z - max_K z) on the kept set, -inf elsewhere.
+ *   9. Selected-token log-prob under the raw logits (TokenSpeed
+ *      "backends/triton.py" page, TritonSamplingBackend._write_logprob_outputs:
+ *      selected_token_logprobs(logits, sampled)): l_id - ln sum_j exp(l_j).
  *
  * Exemption flags (bit 0: the two best perturbed scores are within 1e-5
  * relative; bit 1: a top-p cumulative mass next to the cut is within 1e-5 of
@@ -428,6 +431,47 @@ int oracle_sample(const void* logits, int dtype, int64_t logits_rows, int64_t vo
   jb.out_top2 = out_top2;
   jb.nthreads = nthreads;
   return run_job(&jb, error_word);
+}
+
+/* 9. Log-probability of a chosen token under the raw logits (TokenSpeed
+ * "backends/triton.py" page, TritonSamplingBackend._write_logprob_outputs:
+ * next_token_logprobs = selected_token_logprobs(logits, sampled) -- a function
+ * of the logits and the ids only, so no temperature and no filter apply):
+ * out[i] = l_id - ln sum_j exp(l_j) over row src(i), NaN logits read as -inf.
+ * A row whose maximum is +inf uses its limit distribution (uniform over the
+ * +inf entries).  NaN for an id outside [0, V), a row index out of range or a
+ * row with no finite entry.  Reading of "selected token log-prob": the plain
+ * log-softmax of the logits the sampler was given, in double. */
+int oracle_selected_log_probs(const void* logits, int dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                              int32_t n, const int32_t* gather, const int32_t* ids, double* out) {
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t src = gather ? (int64_t)gather[i] : i;
+    const int64_t id = ids[i];
+    out[i] = NAN;
+    if (src < 0 || src >= logits_rows || id < 0 || id >= vocab) continue;
+    double mx = -INFINITY;
+    int64_t n_inf = 0;
+    for (int64_t j = 0; j < vocab; ++j) {
+      double v = read_logit(logits, dtype, src * row_stride + j);
+      if (isnan(v)) v = -INFINITY;
+      if (v > mx) mx = v;
+      if (v == INFINITY) ++n_inf;
+    }
+    if (mx == -INFINITY) continue;
+    double l_id = read_logit(logits, dtype, src * row_stride + id);
+    if (isnan(l_id)) l_id = -INFINITY;
+    if (mx == INFINITY) {
+      out[i] = l_id == INFINITY ? -log((double)n_inf) : -INFINITY;
+      continue;
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < vocab; ++j) {
+      double v = read_logit(logits, dtype, src * row_stride + j);
+      if (!isnan(v)) sum += exp(v - mx);
+    }
+    out[i] = (l_id - mx) - log(sum);
+  }
+  return 0;
 }
 
 /* Log-probs of the processed distribution for num_rows rows (every row's own

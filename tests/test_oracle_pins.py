@@ -485,6 +485,56 @@ def test_top_p_tie_flag():
 
 
 # --------------------------------------------------------------------------
+# selected-token log-prob under the raw logits
+# --------------------------------------------------------------------------
+def test_selected_log_prob_closed_forms():
+    """Uniform rows give -ln V; a lone finite entry gives 0 (others -inf); two
+    finite entries a, b give -ln(1 + e^(b - a))."""
+    for V in (1, 2, 7, 1000):
+        x = np.full((3, V), 0.25, np.float32)
+        lp = oracle.selected_log_probs(x, F32, [0, V - 1, V // 2])
+        assert np.allclose(lp, -np.log(V), rtol=0, atol=1e-12)
+    x = np.full((1, 6), -np.inf, np.float32)
+    x[0, 4] = 3.5
+    assert oracle.selected_log_probs(x, F32, [4])[0] == 0.0
+    assert oracle.selected_log_probs(x, F32, [1])[0] == -np.inf
+    for a, b in [(0.0, 0.0), (1.0, -2.0), (-3.25, 7.5)]:
+        x = np.full((1, 5), -np.inf, np.float32)
+        x[0, 1], x[0, 3] = a, b
+        got = oracle.selected_log_probs(x, F32, [1])[0]
+        assert abs(got - (-np.log1p(np.exp(b - a)))) < 1e-12
+
+
+def test_selected_log_prob_normalises_and_shifts():
+    """exp of the selected log-probs over every id sums to 1, and adding a
+    constant to the row (exactly representable) changes nothing."""
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((1, 9)) * 3).astype(np.float32)
+    lp = oracle.selected_log_probs(np.repeat(x, 9, axis=0), F32, np.arange(9))
+    assert abs(np.exp(lp).sum() - 1.0) < 1e-12
+    x2 = (x + np.float32(16.0)).astype(np.float32)
+    lp2 = oracle.selected_log_probs(np.repeat(x2, 9, axis=0), F32, np.arange(9))
+    assert np.allclose(lp, lp2, rtol=0, atol=1e-5)  # x + 16 rounds in fp32
+
+
+def test_selected_log_prob_special_values():
+    """NaN is read as -inf; a +inf maximum shares the mass among +inf entries;
+    bad ids and rows give NaN; bf16 rows widen exactly."""
+    x = np.array([[np.nan, 0.0, 0.0]], np.float32)
+    assert abs(oracle.selected_log_probs(x, F32, [1])[0] + np.log(2)) < 1e-15
+    x = np.array([[np.inf, 1.0, np.inf, 2.0]], np.float32)
+    lp = oracle.selected_log_probs(np.repeat(x, 2, axis=0), F32, [0, 3])
+    assert abs(lp[0] + np.log(2)) < 1e-15 and lp[1] == -np.inf
+    assert np.isnan(oracle.selected_log_probs(np.zeros((1, 4), np.float32), F32, [4])[0])
+    assert np.isnan(oracle.selected_log_probs(np.zeros((1, 4), np.float32), F32, [0], gather_indices=[3])[0])
+    assert np.isnan(oracle.selected_log_probs(np.full((1, 4), -np.inf, np.float32), F32, [0])[0])
+    from logits_sampling_gb300 import workloads as W
+    xf = np.array([[1.0, -2.5, 0.375, 3.0]], np.float32)
+    assert np.array_equal(oracle.selected_log_probs(W.to_bf16_bits(xf), oracle.DTYPE_BF16, [2]),
+                          oracle.selected_log_probs(xf, F32, [2]))
+
+
+# --------------------------------------------------------------------------
 # regression anchor
 # --------------------------------------------------------------------------
 def test_tiny_golden_regression():
