@@ -237,9 +237,26 @@ def run_ours(args, world, rank, local):
     t2r = None if w.token_to_request_index is None else torch.from_numpy(w.token_to_request_index).to(device)
     out = torch.empty(w.n, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
+    if args.call != "sample":
+        # ids plus log-prob rows plus the selected token's log-prob: one fused call,
+        # or ls_sample followed by ls_log_probs (two reads of the logits)
+        out_lp = torch.empty((w.n, w.vocab), dtype=torch.float32, device=device)
+        out_sel = torch.empty(w.n, dtype=torch.float32, device=device)
+        if w.spec is not None and t2r is None:
+            D, P, S = w.spec
+            r = np.arange(w.n)
+            t2r = torch.from_numpy(np.where(r < D * (1 + S), r // (1 + S), D + r - D * (1 + S)).astype(np.int32))
+            t2r = t2r.to(device)
 
     def step(i, logits):
-        if w.spec is not None:
+        if args.call == "fused":
+            ls.sample_log_probs(logits, w.n, prm, i, w.no_top_k, w.no_top_p, gather_indices=gather,
+                                token_to_request_index=t2r, out=out, out_log_probs=out_lp, out_selected=out_sel)
+        elif args.call == "separate":
+            ls.sample(logits, w.n, prm, i, w.no_top_k, w.no_top_p, gather_indices=gather,
+                      token_to_request_index=t2r, out=out)
+            ls.log_probs(logits, prm, num_rows=w.n, gather_indices=gather, token_to_request_index=t2r, out=out_lp)
+        elif w.spec is not None:
             D, P, S = w.spec
             ls.sample_speculative(logits, D, P, S, prm, i, w.no_top_k, w.no_top_p, gather_indices=gather, out=out)
         else:
@@ -318,14 +335,18 @@ def run_ours(args, world, rank, local):
 
     peaks, peak_src = measured_peaks()
     alg_bytes = W.algorithmic_bytes(w)
+    if args.call == "fused":  # one read, the log-prob rows written, id + selected log-prob per row
+        alg_bytes = W.algorithmic_bytes(w, with_log_probs=True) + w.n * (28 + 8)
+    elif args.call == "separate":  # the same outputs from two calls: the logits read twice
+        alg_bytes = W.algorithmic_bytes(w) + W.algorithmic_bytes(w, with_log_probs=True)
     achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    traffic = ncu_traffic(args.workload)
+    traffic = ncu_traffic(args.workload) if args.call == "sample" else None
     line = {
         "metric": METRIC, "value": rows_per_s, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.workload], "rows": w.n, "vocab": w.vocab,
+        "config": {"workload": DESCRIPTIONS[args.workload], "rows": w.n, "vocab": w.vocab, "call": args.call,
                    "l2": f"{copies} rotating input copies ({copies * x.numel() * x.element_size() / 1e6:.0f} MB) "
                          f"> 2x L2", "parallelism": f"replicas x{world} (rows independent, no collective)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -337,7 +358,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "source_hash": source_hash(),
     }
-    if rank == 0 and not args.no_cpu:
+    if rank == 0 and not args.no_cpu and args.call == "sample":
         rate, el, done, threads = cpu_oracle_rate(w, target_s=args.cpu_s, max_rows=args.ref_rows)
         line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{done} rows ({min(w.n, args.ref_rows)} of the workload's {w.n} per "
@@ -360,6 +381,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--max-copies", type=int, default=8)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--call", choices=["sample", "fused", "separate"], default="sample",
+                    help="sample: ids (ls_sample); fused: ids, log-prob rows and selected log-probs from one "
+                         "ls_sample_log_probs call; separate: ls_sample then ls_log_probs")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
