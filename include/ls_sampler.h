@@ -5,7 +5,7 @@
  * and computes the per-row log-probs of the processed distribution
  * (temperature, exact top-k, exact top-p).  Every call is asynchronous on the
  * caller's CUDA stream, allocates nothing, never synchronises with the host
- * and launches one kernel.
+ * and launches one kernel (ls_sample_device_step: two).
  *
  * Conventions shared by all entry points
  * --------------------------------------
@@ -148,6 +148,28 @@ ls_status ls_sample_speculative(const void* required_logits, ls_dtype dtype, int
 ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
                        int32_t num_rows, const int32_t* gather_indices, const int32_t* token_to_request_index,
                        const ls_params* params, float* out_log_probs, int32_t* error_word, void* stream);
+
+/*
+ * ls_sample_device_step -- ls_sample with the Philox step word in device
+ * memory, advanced on the device after the call, so that a CUDA graph that
+ * captured the call draws fresh noise at every replay.
+ *
+ * The "core.inference.sampling.flashinfer_sampling" page (FlashInferSampling
+ * class description) runs its sampler eagerly because FlashInfer bakes the
+ * Philox state into a captured graph as a by-value constant, so a captured
+ * sampler replays identical random numbers.  Here the kernel reads *step when
+ * it starts and a second one-thread kernel adds 1 to *step after it on the same
+ * stream (two launches per call).  Rows, ids and errors are exactly those of
+ * ls_sample(..., step = the value *step held, ...).
+ *
+ *   step    device uint64[1], read by the call and left at its value + 1
+ *           (n == 0: nothing is launched and *step is unchanged)
+ * Other arguments as for ls_sample.
+ */
+ls_status ls_sample_device_step(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
+                                int64_t row_stride, int32_t n, const int32_t* gather_indices,
+                                const int32_t* token_to_request_index, const ls_params* params, uint64_t* step,
+                                int no_top_k, int no_top_p, int32_t* out_ids, int32_t* error_word, void* stream);
 
 /*
  * ls_sample_log_probs -- sample n token ids and, from the same single read of

@@ -2,8 +2,8 @@
 
 The binding only marshals arguments (torch tensors -> device pointers, the
 current CUDA stream) and calls the C ABI declared in include/ls_sampler.h:
-``ls_sample``, ``ls_sample_speculative``, ``ls_log_probs`` and
-``ls_sample_log_probs``.  Every step of the
+``ls_sample``, ``ls_sample_speculative``, ``ls_log_probs``,
+``ls_sample_log_probs`` and ``ls_sample_device_step``.  Every step of the
 sampling path runs in the library's CUDA kernels; there is no CPU fallback.
 If the library has not been built (``python -m logits_sampling_gb300.build``)
 or no CUDA device is present, the calls raise.
@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     log_probs,
     max_vocab,
     sample,
+    sample_device_step,
     sample_log_probs,
     sample_speculative,
     status_string,

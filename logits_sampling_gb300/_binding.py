@@ -48,6 +48,8 @@ def load_library():
     lib.ls_log_probs.restype = ci
     lib.ls_sample_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P, P, P]
     lib.ls_sample_log_probs.restype = ci
+    lib.ls_sample_device_step.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, ci, ci, P, P, P]
+    lib.ls_sample_device_step.restype = ci
     lib.ls_status_string.argtypes = [ci]
     lib.ls_status_string.restype = ctypes.c_char_p
     lib.ls_max_vocab.argtypes = [ci]
@@ -237,3 +239,25 @@ def sample_log_probs(logits, n, params, step, no_top_k, no_top_p, gather_indices
     if st != LS_OK:
         raise LSError(st, "ls_sample_log_probs")
     return out, out_log_probs, out_selected
+
+
+def sample_device_step(logits, n, params, step, no_top_k, no_top_p, gather_indices=None,
+                       token_to_request_index=None, out=None, error_word=None, stream=None):
+    """ls_sample_device_step: `step` is a device int64/uint64 tensor of one
+    element, read by the call and advanced by one on the device (graph-safe).
+    Returns out (int32 [n])."""
+    import torch
+    lib = load_library()
+    ptr, dt, rows, V, stride = _logits_desc(logits)
+    if step.dtype not in (torch.int64, torch.uint64) or step.numel() != 1:
+        raise TypeError("step must be a one-element int64/uint64 device tensor")
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=logits.device)
+    prm = params.as_struct()
+    st = lib.ls_sample_device_step(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
+                                   _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
+                                   _dptr(step), int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"),
+                                   _i32(error_word, "error_word"), _stream(stream))
+    if st != LS_OK:
+        raise LSError(st, "ls_sample_device_step")
+    return out

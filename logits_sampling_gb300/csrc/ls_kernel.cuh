@@ -56,6 +56,7 @@ struct KernelArgs {
   const uint64_t* seed;
   int32_t num_requests;
   uint64_t step;
+  const uint64_t* step_ptr;  // when not NULL the step word is read from device memory
   int32_t* out_ids;
   int32_t* out_t2r;
   float* out_lp;   // log-prob rows (MODE_LOGPROBS; MODE_BOTH when not NULL)
@@ -841,6 +842,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   }
   // ---- one block reduction: row maximum, total mass, top-k bound --------
   const uint64_t seed = kSample ? a.seed[req] : 0ull;  // its latency overlaps the reduction
+  const uint64_t step = kSample && a.step_ptr ? *a.step_ptr : a.step;
   // Each warp reduces its maximum, rescales every lane's sum to the warp's
   // reference RN(max * c) and adds; after one barrier every warp combines the
   // 16 warp results the same way (fixed order, so S is deterministic and the
@@ -1088,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // barriers); only more than kTieList ties take a pass over the list.
   const int nties = ties_in_take && lc <= M ? sh.tie_count : -1;
   if (nties >= 0 && nties <= kTieList) {
-    if (tid < nties) score_entry(&sh.best, M, T, seed, a.step, (uint32_t)i, sh.tie_j[tid]);
+    if (tid < nties) score_entry(&sh.best, M, T, seed, step, (uint32_t)i, sh.tie_j[tid]);
   } else if (tie_only || kSample) {
     cs.each(M, [&](float x, int64_t j) {
       if (MODE != MODE_SAMPLE && tie_only) atomicAdd(&sh.acc[0], 1u);
@@ -1097,7 +1099,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
           atomicMin(&sh.min_index, (int)j);
         } else {
           const float z = M == kPosInf ? 0.f : __fdiv_rn(x, T);
-          atomicMax(&sh.best, argmax_key(z + gumbel_of_word(noise_word(seed, a.step, (uint32_t)i, j)), j));
+          atomicMax(&sh.best, argmax_key(z + gumbel_of_word(noise_word(seed, step, (uint32_t)i, j)), j));
         }
       }
     });
@@ -1145,7 +1147,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
 
   if (kSample) {
     // ---- Gumbel-max over the kept set ------------------------------------
-    gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, seed, a.step, (uint32_t)i);
+    gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, seed, step, (uint32_t)i);
     if (tid == 0) {
       const int32_t id = argmax_index(sh.best);
       a.out_ids[i] = id;

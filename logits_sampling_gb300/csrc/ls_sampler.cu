@@ -8,6 +8,10 @@ namespace lsg {
 extern template ls_status dispatch<MODE_SAMPLE>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
 extern template ls_status dispatch<MODE_LOGPROBS>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
 extern template ls_status dispatch<MODE_BOTH>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
+
+// Advances a device-resident Philox step word after the sampler that read it
+// (stream order: every CTA of the sampler has read the word before this runs).
+__global__ void advance_step_kernel(uint64_t* step) { *step += 1ull; }
 }  // namespace lsg
 
 using namespace lsg;
@@ -74,6 +78,29 @@ ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, 
   a.map_mode = token_to_request_index ? MAP_T2R : MAP_IDENTITY;
   a.out_lp = out_log_probs;
   return dispatch<MODE_LOGPROBS>(a, dtype, ROUTE_KP, num_rows, static_cast<cudaStream_t>(stream));
+}
+
+ls_status ls_sample_device_step(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
+                                int64_t row_stride, int32_t n, const int32_t* gather_indices,
+                                const int32_t* token_to_request_index, const ls_params* params, uint64_t* step,
+                                int no_top_k, int no_top_p, int32_t* out_ids, int32_t* error_word, void* stream) {
+  if (n < 0 || !step) return LS_ERR_INVALID_ARG;
+  if (n == 0) return LS_OK;
+  if (!common_ok(logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, true) || !out_ids)
+    return LS_ERR_INVALID_ARG;
+  if (!gather_indices && (int64_t)n > logits_rows) return LS_ERR_INVALID_ARG;
+  if (!token_to_request_index && n > params->num_requests) return LS_ERR_INVALID_ARG;
+  KernelArgs a = make_args(logits, logits_rows, vocab, row_stride, gather_indices, params, 0, error_word);
+  a.step_ptr = step;
+  a.t2r = token_to_request_index;
+  a.map_mode = token_to_request_index ? MAP_T2R : MAP_IDENTITY;
+  a.out_ids = out_ids;
+  const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const ls_status rc = dispatch<MODE_SAMPLE>(a, dtype, route, n, st);
+  if (rc != LS_OK) return rc;
+  advance_step_kernel<<<1, 1, 0, st>>>(step);
+  return cudaGetLastError() == cudaSuccess ? LS_OK : LS_ERR_CUDA;
 }
 
 ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,

@@ -31,7 +31,8 @@ def _declared_functions():
 
 def test_header_declares_the_calls():
     names = _declared_functions()
-    assert {"ls_sample", "ls_sample_speculative", "ls_log_probs", "ls_sample_log_probs", "ls_status_string"} <= names
+    assert {"ls_sample", "ls_sample_speculative", "ls_log_probs", "ls_sample_log_probs", "ls_sample_device_step",
+            "ls_status_string"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -88,6 +89,12 @@ def test_host_validation_before_any_launch(lib):
     assert f(fake, 1, 4, 10, 10, 2, None, None, byref(prm), 0, 0, 0, None, fake, fake, None, None) == 1
     assert f(fake, 1, 4, 10, 10, 5, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, None) == 1
     assert f(fake, 1, 4, 10, 10, 3, None, None, byref(prm2), 0, 0, 0, fake, None, fake, None, None) == 1
+    # device step word: the ls_sample checks, and the step pointer is required
+    d = lib.ls_sample_device_step
+    assert d(fake, 1, 4, 10, 10, 2, None, None, byref(prm), None, 0, 0, fake, None, None) == 1
+    assert d(fake, 1, 4, 10, 10, -1, None, None, byref(prm), fake, 0, 0, fake, None, None) == 1
+    assert d(fake, 1, 4, 10, 10, 0, None, None, byref(prm), fake, 0, 0, fake, None, None) == 0
+    assert d(fake, 1, 4, 10, 10, 5, None, None, byref(prm), fake, 0, 0, fake, None, None) == 1
 
 
 def test_status_strings(lib):
