@@ -249,7 +249,9 @@ def run_ours(args, world, rank, local):
             t2r = t2r.to(device)
 
     def step(i, logits):
-        if args.call == "fused":
+        if args.call == "argmax":
+            ls.argmax(logits, n=w.n, gather_indices=gather, out=out)
+        elif args.call == "fused":
             ls.sample_log_probs(logits, w.n, prm, i, w.no_top_k, w.no_top_p, gather_indices=gather,
                                 token_to_request_index=t2r, out=out, out_log_probs=out_lp, out_selected=out_sel)
         elif args.call == "separate":
@@ -335,7 +337,9 @@ def run_ours(args, world, rank, local):
 
     peaks, peak_src = measured_peaks()
     alg_bytes = W.algorithmic_bytes(w)
-    if args.call == "fused":  # one read, the log-prob rows written, id + selected log-prob per row
+    if args.call == "argmax":  # the rows read once, an id written per row (no parameters)
+        alg_bytes = w.n * w.vocab * w.elem_bytes + w.n * (4 + (4 if w.gather_indices is not None else 0))
+    elif args.call == "fused":  # one read, the log-prob rows written, id + selected log-prob per row
         alg_bytes = W.algorithmic_bytes(w, with_log_probs=True) + w.n * (28 + 8)
     elif args.call == "separate":  # the same outputs from two calls: the logits read twice
         alg_bytes = W.algorithmic_bytes(w) + W.algorithmic_bytes(w, with_log_probs=True)
@@ -381,9 +385,10 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--max-copies", type=int, default=8)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--call", choices=["sample", "fused", "separate"], default="sample",
+    ap.add_argument("--call", choices=["sample", "fused", "separate", "argmax"], default="sample",
                     help="sample: ids (ls_sample); fused: ids, log-prob rows and selected log-probs from one "
-                         "ls_sample_log_probs call; separate: ls_sample then ls_log_probs")
+                         "ls_sample_log_probs call; separate: ls_sample then ls_log_probs; argmax: the "
+                         "all-greedy fast path (ls_argmax) on the workload's rows")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

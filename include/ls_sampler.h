@@ -202,6 +202,24 @@ ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits
                               int no_top_k, int no_top_p, int32_t* out_ids, float* out_log_probs,
                               float* out_selected_log_probs, int32_t* error_word, void* stream);
 
+/*
+ * ls_argmax -- the all-greedy fast path: out_ids[i] = the lowest index of the
+ * maximum of logits row i (row gather_indices[i] when given).
+ *
+ * Follows the TokenSpeed "backends/triton.py" page (TritonSamplingBackend.
+ * sample and verify: when every request of the batch is greedy, the argmax of
+ * the logits replaces the sampling kernels).  The ids are the ones ls_sample
+ * returns for greedy rows (T < 1e-5): NaN read as -inf, ties to the lowest
+ * index; a row with no entry above -inf gives -1 and LS_ROW_ERR_NO_FINITE, a
+ * gather index out of range -1 and LS_ROW_ERR_BAD_GATHER.  No parameters, no
+ * noise; one streaming read of each row.
+ *
+ *   out_ids   device int32[n]
+ * Other arguments as for ls_sample.
+ */
+ls_status ls_argmax(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                    int32_t n, const int32_t* gather_indices, int32_t* out_ids, int32_t* error_word, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* ls_status_string(ls_status s);
 

@@ -3,7 +3,7 @@
 The binding only marshals arguments (torch tensors -> device pointers, the
 current CUDA stream) and calls the C ABI declared in include/ls_sampler.h:
 ``ls_sample``, ``ls_sample_speculative``, ``ls_log_probs``,
-``ls_sample_log_probs`` and ``ls_sample_device_step``.  Every step of the
+``ls_sample_log_probs``, ``ls_sample_device_step`` and ``ls_argmax``.  Every step of the
 sampling path runs in the library's CUDA kernels; there is no CPU fallback.
 If the library has not been built (``python -m logits_sampling_gb300.build``)
 or no CUDA device is present, the calls raise.
@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     LS_ROW_ERR_NO_FINITE,
     LSError,
     SamplingParams,
+    argmax,
     lib_path,
     load_library,
     log_probs,

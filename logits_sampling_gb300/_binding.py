@@ -50,6 +50,8 @@ def load_library():
     lib.ls_sample_log_probs.restype = ci
     lib.ls_sample_device_step.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, ci, ci, P, P, P]
     lib.ls_sample_device_step.restype = ci
+    lib.ls_argmax.argtypes = [P, ci, i64, i64, i64, i32, P, P, P, P]
+    lib.ls_argmax.restype = ci
     lib.ls_status_string.argtypes = [ci]
     lib.ls_status_string.restype = ctypes.c_char_p
     lib.ls_max_vocab.argtypes = [ci]
@@ -260,4 +262,21 @@ def sample_device_step(logits, n, params, step, no_top_k, no_top_p, gather_indic
                                    _i32(error_word, "error_word"), _stream(stream))
     if st != LS_OK:
         raise LSError(st, "ls_sample_device_step")
+    return out
+
+
+def argmax(logits, n=None, gather_indices=None, out=None, error_word=None, stream=None):
+    """ls_argmax: the lowest index of each row's maximum (all-greedy batches).
+    Returns out (int32 [n])."""
+    import torch
+    lib = load_library()
+    ptr, dt, rows, V, stride = _logits_desc(logits)
+    if n is None:
+        n = len(gather_indices) if gather_indices is not None else rows
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=logits.device)
+    st = lib.ls_argmax(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"), _i32(out, "out"),
+                       _i32(error_word, "error_word"), _stream(stream))
+    if st != LS_OK:
+        raise LSError(st, "ls_argmax")
     return out

@@ -32,7 +32,7 @@ def _declared_functions():
 def test_header_declares_the_calls():
     names = _declared_functions()
     assert {"ls_sample", "ls_sample_speculative", "ls_log_probs", "ls_sample_log_probs", "ls_sample_device_step",
-            "ls_status_string"} <= names
+            "ls_argmax", "ls_status_string"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -95,6 +95,12 @@ def test_host_validation_before_any_launch(lib):
     assert d(fake, 1, 4, 10, 10, -1, None, None, byref(prm), fake, 0, 0, fake, None, None) == 1
     assert d(fake, 1, 4, 10, 10, 0, None, None, byref(prm), fake, 0, 0, fake, None, None) == 0
     assert d(fake, 1, 4, 10, 10, 5, None, None, byref(prm), fake, 0, 0, fake, None, None) == 1
+    # greedy fast path
+    assert lib.ls_argmax(fake, 1, 4, 10, 10, -1, None, fake, None, None) == 1
+    assert lib.ls_argmax(fake, 1, 4, 10, 10, 0, None, fake, None, None) == 0
+    assert lib.ls_argmax(fake, 1, 4, 10, 10, 2, None, None, None, None) == 1
+    assert lib.ls_argmax(fake, 1, 4, 10, 10, 5, None, fake, None, None) == 1
+    assert lib.ls_argmax(None, 1, 4, 10, 10, 2, None, fake, None, None) == 1
 
 
 def test_status_strings(lib):
