@@ -248,8 +248,31 @@ def run_ours(args, world, rank, local):
             t2r = torch.from_numpy(np.where(r < D * (1 + S), r // (1 + S), D + r - D * (1 + S)).astype(np.int32))
             t2r = t2r.to(device)
 
+    if args.call == "verify":
+        # the decode requests' verify rows: sample them, then verify random drafts
+        if w.spec is None:
+            raise SystemExit("--call verify needs the speculative workload")
+        D, _, S = w.spec
+        vn = D * (1 + S)
+        vgather = gather[:vn] if gather is not None else None
+        cand = torch.from_numpy(np.random.default_rng(0).integers(0, w.vocab, (D, 1 + S)).astype(np.int32)).to(device)
+        vtarget = torch.empty(vn, dtype=torch.int32, device=device)
+        vpred = torch.empty(vn, dtype=torch.int32, device=device)
+        vai = torch.empty(vn, dtype=torch.int32, device=device)
+        van = torch.empty(D, dtype=torch.int32, device=device)
+        vprm = prm.as_struct()
+        vlib = ls.load_library()
+        import ctypes
+        from logits_sampling_gb300._binding import _dptr, _logits_desc, _stream
+
     def step(i, logits):
-        if args.call == "argmax":
+        if args.call == "verify":
+            ptr, dt, rows_, V_, stride_ = _logits_desc(logits)
+            st = vlib.ls_sample_verify(ptr, dt, rows_, V_, stride_, D, 1 + S, _dptr(vgather), ctypes.byref(vprm), i,
+                                       int(w.no_top_k), int(w.no_top_p), _dptr(cand), _dptr(vtarget), _dptr(vpred),
+                                       _dptr(vai), _dptr(van), None, _stream(None))
+            assert st == 0, st
+        elif args.call == "argmax":
             ls.argmax(logits, n=w.n, gather_indices=gather, out=out)
         elif args.call == "fused":
             ls.sample_log_probs(logits, w.n, prm, i, w.no_top_k, w.no_top_p, gather_indices=gather,
@@ -337,7 +360,11 @@ def run_ours(args, world, rank, local):
 
     peaks, peak_src = measured_peaks()
     alg_bytes = W.algorithmic_bytes(w)
-    if args.call == "argmax":  # the rows read once, an id written per row (no parameters)
+    if args.call == "verify":  # the decode verify rows read once; ids, drafts, predicts, accept outputs
+        D, _, S = w.spec
+        vn = D * (1 + S)
+        alg_bytes = vn * w.vocab * w.elem_bytes + vn * (28 + 4 + 4 + 4 + 4) + D * 4
+    elif args.call == "argmax":  # the rows read once, an id written per row (no parameters)
         alg_bytes = w.n * w.vocab * w.elem_bytes + w.n * (4 + (4 if w.gather_indices is not None else 0))
     elif args.call == "fused":  # one read, the log-prob rows written, id + selected log-prob per row
         alg_bytes = W.algorithmic_bytes(w, with_log_probs=True) + w.n * (28 + 8)
@@ -385,10 +412,11 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--max-copies", type=int, default=8)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--call", choices=["sample", "fused", "separate", "argmax"], default="sample",
+    ap.add_argument("--call", choices=["sample", "fused", "separate", "argmax", "verify"], default="sample",
                     help="sample: ids (ls_sample); fused: ids, log-prob rows and selected log-probs from one "
                          "ls_sample_log_probs call; separate: ls_sample then ls_log_probs; argmax: the "
-                         "all-greedy fast path (ls_argmax) on the workload's rows")
+                         "all-greedy fast path (ls_argmax) on the workload's rows; verify: ls_sample_verify on "
+                         "the speculative workload's decode rows")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

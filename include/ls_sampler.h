@@ -5,7 +5,7 @@
  * and computes the per-row log-probs of the processed distribution
  * (temperature, exact top-k, exact top-p).  Every call is asynchronous on the
  * caller's CUDA stream, allocates nothing, never synchronises with the host
- * and launches one kernel (ls_sample_device_step: two).
+ * and launches one kernel (ls_sample_device_step and ls_sample_verify: two).
  *
  * Conventions shared by all entry points
  * --------------------------------------
@@ -219,6 +219,51 @@ ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits
  */
 ls_status ls_argmax(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
                     int32_t n, const int32_t* gather_indices, int32_t* out_ids, int32_t* error_word, void* stream);
+
+/*
+ * ls_verify_chain -- speculative chain verification against the target
+ * model's sampled tokens.
+ *
+ * Follows the TokenSpeed "backends/triton.py" page (TritonSamplingBackend.
+ * verify: verify_chain_target_sampled(predicts, accept_index,
+ * accept_token_num, candidates, target_sampled), then accept_length += 1).
+ * The pages print only the call; the rule implemented (the plain chain rule):
+ * request b has n = num_tokens positions; candidates[b, 0] is the token the
+ * drafts extend, candidates[b, j] (j >= 1) the j-th draft, and
+ * target_sampled[b*n + j] the target's token after position j.  Position 0 is
+ * always accepted; position j >= 1 is accepted while every earlier position
+ * was and candidates[b, j] == target_sampled[b*n + j - 1].  For an accepted
+ * position accept_index[b, j] = b*n + j and predicts[b*n + j] =
+ * target_sampled[b*n + j]; other accept_index entries are -1 and other
+ * predicts are left unchanged.  accept_token_num[b] = the number of accepted
+ * drafts (the page's accept_length is that + 1: the bonus token).
+ *
+ *   candidates        device int32[bs * num_tokens] (row-major [bs, n])
+ *   target_sampled    device int32[bs * num_tokens]
+ *   predicts          device int32[bs * num_tokens]
+ *   accept_index      device int32[bs * num_tokens]
+ *   accept_token_num  device int32[bs]
+ * bs = 0: nothing launched.  num_tokens >= 1.
+ */
+ls_status ls_verify_chain(const int32_t* candidates, const int32_t* target_sampled, int32_t bs,
+                          int32_t num_tokens, int32_t* predicts, int32_t* accept_index, int32_t* accept_token_num,
+                          void* stream);
+
+/*
+ * ls_sample_verify -- sample the verify rows of bs decode requests
+ * (num_tokens rows each: ls_sample_speculative with num_decode = bs,
+ * num_prefill = 0, num_speculative_tokens = num_tokens - 1) into
+ * out_target_sampled, then ls_verify_chain on them: two launches, no host
+ * round trip between the target's sampling and the acceptance.
+ *
+ *   out_target_sampled  device int32[bs * num_tokens]: the sampled verify rows
+ * Other arguments as for ls_sample_speculative and ls_verify_chain.
+ */
+ls_status ls_sample_verify(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
+                           int32_t bs, int32_t num_tokens, const int32_t* gather_indices, const ls_params* params,
+                           uint64_t step, int no_top_k, int no_top_p, const int32_t* candidates,
+                           int32_t* out_target_sampled, int32_t* predicts, int32_t* accept_index,
+                           int32_t* accept_token_num, int32_t* error_word, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* ls_status_string(ls_status s);

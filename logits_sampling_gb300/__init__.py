@@ -3,7 +3,8 @@
 The binding only marshals arguments (torch tensors -> device pointers, the
 current CUDA stream) and calls the C ABI declared in include/ls_sampler.h:
 ``ls_sample``, ``ls_sample_speculative``, ``ls_log_probs``,
-``ls_sample_log_probs``, ``ls_sample_device_step`` and ``ls_argmax``.  Every step of the
+``ls_sample_log_probs``, ``ls_sample_device_step``, ``ls_argmax``,
+``ls_verify_chain`` and ``ls_sample_verify``.  Every step of the
 sampling path runs in the library's CUDA kernels; there is no CPU fallback.
 If the library has not been built (``python -m logits_sampling_gb300.build``)
 or no CUDA device is present, the calls raise.
@@ -25,5 +26,7 @@ from ._binding import (  # noqa: F401
     sample_device_step,
     sample_log_probs,
     sample_speculative,
+    sample_verify,
     status_string,
+    verify_chain,
 )

@@ -52,6 +52,10 @@ def load_library():
     lib.ls_sample_device_step.restype = ci
     lib.ls_argmax.argtypes = [P, ci, i64, i64, i64, i32, P, P, P, P]
     lib.ls_argmax.restype = ci
+    lib.ls_verify_chain.argtypes = [P, P, i32, i32, P, P, P, P]
+    lib.ls_verify_chain.restype = ci
+    lib.ls_sample_verify.argtypes = [P, ci, i64, i64, i64, i32, i32, P, PP, u64, ci, ci, P, P, P, P, P, P, P]
+    lib.ls_sample_verify.restype = ci
     lib.ls_status_string.argtypes = [ci]
     lib.ls_status_string.restype = ctypes.c_char_p
     lib.ls_max_vocab.argtypes = [ci]
@@ -280,3 +284,50 @@ def argmax(logits, n=None, gather_indices=None, out=None, error_word=None, strea
     if st != LS_OK:
         raise LSError(st, "ls_argmax")
     return out
+
+
+def verify_chain(candidates, target_sampled, predicts=None, accept_index=None, accept_token_num=None, stream=None):
+    """ls_verify_chain: candidates int32 [bs, n] and target_sampled int32 [bs * n]
+    on the device.  Returns (predicts [bs * n], accept_index [bs, n],
+    accept_token_num [bs])."""
+    import torch
+    lib = load_library()
+    bs, n = candidates.shape
+    dev = candidates.device
+    if predicts is None:
+        predicts = torch.full((bs * n,), -1, dtype=torch.int32, device=dev)
+    if accept_index is None:
+        accept_index = torch.empty((bs, n), dtype=torch.int32, device=dev)
+    if accept_token_num is None:
+        accept_token_num = torch.empty(bs, dtype=torch.int32, device=dev)
+    st = lib.ls_verify_chain(_i32(candidates.contiguous(), "candidates"), _i32(target_sampled, "target_sampled"),
+                             int(bs), int(n), _i32(predicts, "predicts"), _i32(accept_index, "accept_index"),
+                             _i32(accept_token_num, "accept_token_num"), _stream(stream))
+    if st != LS_OK:
+        raise LSError(st, "ls_verify_chain")
+    return predicts, accept_index, accept_token_num
+
+
+def sample_verify(logits, candidates, params, step, no_top_k, no_top_p, gather_indices=None, error_word=None,
+                  stream=None):
+    """ls_sample_verify: sample the bs * n verify rows, then verify the chains.
+    Returns (target_sampled, predicts, accept_index, accept_token_num)."""
+    import torch
+    lib = load_library()
+    ptr, dt, rows, V, stride = _logits_desc(logits)
+    bs, n = candidates.shape
+    dev = logits.device
+    target = torch.empty(bs * n, dtype=torch.int32, device=dev)
+    predicts = torch.full((bs * n,), -1, dtype=torch.int32, device=dev)
+    accept_index = torch.empty((bs, n), dtype=torch.int32, device=dev)
+    accept_token_num = torch.empty(bs, dtype=torch.int32, device=dev)
+    prm = params.as_struct()
+    st = lib.ls_sample_verify(ptr, dt, rows, V, stride, int(bs), int(n), _i32(gather_indices, "gather_indices"),
+                              ctypes.byref(prm), int(step), int(bool(no_top_k)), int(bool(no_top_p)),
+                              _i32(candidates.contiguous(), "candidates"), _i32(target, "target"),
+                              _i32(predicts, "predicts"), _i32(accept_index, "accept_index"),
+                              _i32(accept_token_num, "accept_token_num"), _i32(error_word, "error_word"),
+                              _stream(stream))
+    if st != LS_OK:
+        raise LSError(st, "ls_sample_verify")
+    return target, predicts, accept_index, accept_token_num

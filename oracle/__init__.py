@@ -56,6 +56,8 @@ def _load():
         lib.oracle_log_probs.restype = ctypes.c_int
         lib.oracle_selected_log_probs.argtypes = [P, ctypes.c_int, i64, i64, i64, i32, P, P, P]
         lib.oracle_selected_log_probs.restype = ctypes.c_int
+        lib.oracle_verify_chain.argtypes = [P, P, i32, i32, P, P, P]
+        lib.oracle_verify_chain.restype = None
         _lib = lib
     return _lib
 
@@ -180,3 +182,18 @@ def selected_log_probs(logits, dtype, ids, gather_indices=None, vocab=None):
     out = np.zeros(len(ids), dtype=np.float64)
     _load().oracle_selected_log_probs(_ptr(a), dtype, rows, V, stride, len(ids), _ptr(g), _ptr(ids), _ptr(out))
     return out
+
+
+def verify_chain(candidates, target_sampled, predicts_init=None):
+    """Reference chain verification.  candidates int32 [bs, n], target_sampled
+    int32 [bs * n]; returns predicts [bs * n] (predicts_init where not accepted),
+    accept_index [bs, n] and accept_token_num [bs]."""
+    c = np.ascontiguousarray(candidates, dtype=np.int32)
+    bs, n = c.shape
+    t = np.ascontiguousarray(target_sampled, dtype=np.int32).reshape(-1)
+    pred = (np.full(bs * n, -7, np.int32) if predicts_init is None
+            else np.ascontiguousarray(predicts_init, dtype=np.int32).copy())
+    ai = np.zeros((bs, n), np.int32)
+    an = np.zeros(bs, np.int32)
+    _load().oracle_verify_chain(_ptr(c), _ptr(t), bs, n, _ptr(pred), _ptr(ai), _ptr(an))
+    return pred, ai, an

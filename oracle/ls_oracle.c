@@ -38,6 +38,8 @@
  *   9. Selected-token log-prob under the raw logits (TokenSpeed
  *      "backends/triton.py" page, TritonSamplingBackend._write_logprob_outputs:
  *      selected_token_logprobs(logits, sampled)): l_id - ln sum_j exp(l_j).
+ *  10. Speculative chain verification against the target's sampled tokens
+ *      (TokenSpeed "backends/triton.py" page, TritonSamplingBackend.verify).
  *
  * Exemption flags (bit 0: the two best perturbed scores are within 1e-5
  * relative; bit 1: a top-p cumulative mass next to the cut is within 1e-5 of
@@ -472,6 +474,35 @@ int oracle_selected_log_probs(const void* logits, int dtype, int64_t logits_rows
     out[i] = (l_id - mx) - log(sum);
   }
   return 0;
+}
+
+/* 10. Chain verification of speculative drafts against the target's sampled
+ * tokens (TokenSpeed "backends/triton.py" page, TritonSamplingBackend.verify:
+ * verify_chain_target_sampled(predicts, accept_index, accept_token_num,
+ * candidates, target_sampled), then accept_length += 1).  The pages print only
+ * the call; reading taken (the plain chain rule): request b has n = num_tokens
+ * positions; candidates[b, 0] is the token the drafts extend and
+ * candidates[b, j] (j >= 1) the j-th draft; target_sampled[b*n + j] is the
+ * target's token after position j.  Position 0 is always accepted; position j
+ * >= 1 is accepted while every earlier one was and candidates[b, j] equals
+ * target_sampled[b*n + j - 1].  For an accepted position: accept_index[b, j] =
+ * b*n + j and predicts[b*n + j] = target_sampled[b*n + j]; accept_token_num[b]
+ * = the number of accepted drafts (positions >= 1).  Other entries of
+ * accept_index are -1; other predicts are left as they were. */
+void oracle_verify_chain(const int32_t* candidates, const int32_t* target_sampled, int32_t bs, int32_t n,
+                         int32_t* predicts, int32_t* accept_index, int32_t* accept_token_num) {
+  for (int32_t b = 0; b < bs; ++b) {
+    for (int32_t j = 0; j < n; ++j) accept_index[(int64_t)b * n + j] = -1;
+    int32_t acc = 0;
+    for (int32_t j = 0; j < n; ++j) {
+      const int64_t r = (int64_t)b * n + j;
+      if (j > 0 && candidates[r] != target_sampled[r - 1]) break;
+      accept_index[r] = (int32_t)r;
+      predicts[r] = target_sampled[r];
+      if (j > 0) ++acc;
+    }
+    accept_token_num[b] = acc;
+  }
 }
 
 /* Log-probs of the processed distribution for num_rows rows (every row's own

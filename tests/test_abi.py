@@ -32,7 +32,7 @@ def _declared_functions():
 def test_header_declares_the_calls():
     names = _declared_functions()
     assert {"ls_sample", "ls_sample_speculative", "ls_log_probs", "ls_sample_log_probs", "ls_sample_device_step",
-            "ls_argmax", "ls_status_string"} <= names
+            "ls_argmax", "ls_verify_chain", "ls_sample_verify", "ls_status_string"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -101,6 +101,17 @@ def test_host_validation_before_any_launch(lib):
     assert lib.ls_argmax(fake, 1, 4, 10, 10, 2, None, None, None, None) == 1
     assert lib.ls_argmax(fake, 1, 4, 10, 10, 5, None, fake, None, None) == 1
     assert lib.ls_argmax(None, 1, 4, 10, 10, 2, None, fake, None, None) == 1
+    # chain verification
+    v = lib.ls_verify_chain
+    assert v(fake, fake, -1, 2, fake, fake, fake, None) == 1
+    assert v(fake, fake, 3, 0, fake, fake, fake, None) == 1
+    assert v(fake, fake, 0, 2, fake, fake, fake, None) == 0
+    assert v(fake, None, 3, 2, fake, fake, fake, None) == 1
+    sv = lib.ls_sample_verify
+    assert sv(fake, 1, 100, 10, 10, 2, 3, None, byref(prm), 0, 0, 0, None, fake, fake, fake, fake, None, None) == 1
+    assert sv(fake, 1, 100, 10, 10, 5, 3, None, byref(prm), 0, 0, 0, fake, fake, fake, fake, fake, None, None) == 1
+    assert sv(fake, 1, 5, 10, 10, 2, 3, None, byref(prm), 0, 0, 0, fake, fake, fake, fake, fake, None, None) == 1
+    assert sv(fake, 1, 100, 10, 10, 0, 3, None, byref(prm), 0, 0, 0, fake, fake, fake, fake, fake, None, None) == 0
 
 
 def test_status_strings(lib):

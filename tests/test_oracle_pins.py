@@ -535,6 +535,46 @@ def test_selected_log_prob_special_values():
 
 
 # --------------------------------------------------------------------------
+# speculative chain verification
+# --------------------------------------------------------------------------
+def test_verify_chain_hand_cases():
+    """Request 0: every draft matches the previous target token (all three
+    accepted); request 1: the first draft misses (none); request 2: the second
+    draft misses (one); request 3: a later match after a miss does not count."""
+    cand = np.array([[5, 10, 11, 12],
+                     [5, 99, 11, 12],
+                     [5, 20, 98, 22],
+                     [5, 30, 0, 32]], np.int32)
+    tgt = np.array([10, 11, 12, 13,
+                    40, 41, 42, 43,
+                    20, 21, 22, 23,
+                    31, 32, 33, 34], np.int32)
+    pred, ai, an = oracle.verify_chain(cand, tgt)
+    assert an.tolist() == [3, 0, 1, 0]
+    assert ai.tolist() == [[0, 1, 2, 3], [4, -1, -1, -1], [8, 9, -1, -1], [12, -1, -1, -1]]
+    assert pred.tolist() == [10, 11, 12, 13, 40, -7, -7, -7, 20, 21, -7, -7, 31, -7, -7, -7]
+
+
+def test_verify_chain_single_position_and_brute_force():
+    """n = 1 accepts only the root; for random small cases the accepted count is
+    the length of the matching prefix, found here by direct comparison."""
+    pred, ai, an = oracle.verify_chain(np.array([[3], [4]], np.int32), np.array([8, 9], np.int32))
+    assert an.tolist() == [0, 0] and ai.tolist() == [[0], [1]] and pred.tolist() == [8, 9]
+    rng = np.random.default_rng(2)
+    for _ in range(50):
+        bs, n = rng.integers(1, 5), rng.integers(1, 6)
+        cand = rng.integers(0, 3, (bs, n)).astype(np.int32)
+        tgt = rng.integers(0, 3, bs * n).astype(np.int32)
+        _, ai, an = oracle.verify_chain(cand, tgt)
+        for b in range(bs):
+            k = 0
+            while k + 1 < n and cand[b, k + 1] == tgt[b * n + k]:
+                k += 1
+            assert an[b] == k
+            assert (ai[b] >= 0).sum() == k + 1
+
+
+# --------------------------------------------------------------------------
 # regression anchor
 # --------------------------------------------------------------------------
 def test_tiny_golden_regression():
