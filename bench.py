@@ -252,14 +252,15 @@ def run_ours(args, world, rank, local):
         # the decode requests' verify rows: sample them, then verify random drafts
         if w.spec is None:
             raise SystemExit("--call verify needs the speculative workload")
-        D, _, S = w.spec
-        vn = D * (1 + S)
+        VD, _, VS = w.spec
+        vn = VD * (1 + VS)
         vgather = gather[:vn] if gather is not None else None
-        cand = torch.from_numpy(np.random.default_rng(0).integers(0, w.vocab, (D, 1 + S)).astype(np.int32)).to(device)
+        cand = torch.from_numpy(np.random.default_rng(0).integers(0, w.vocab, (VD, 1 + VS)).astype(np.int32))
+        cand = cand.to(device)
         vtarget = torch.empty(vn, dtype=torch.int32, device=device)
         vpred = torch.empty(vn, dtype=torch.int32, device=device)
         vai = torch.empty(vn, dtype=torch.int32, device=device)
-        van = torch.empty(D, dtype=torch.int32, device=device)
+        van = torch.empty(VD, dtype=torch.int32, device=device)
         vprm = prm.as_struct()
         vlib = ls.load_library()
         import ctypes
@@ -268,7 +269,7 @@ def run_ours(args, world, rank, local):
     def step(i, logits):
         if args.call == "verify":
             ptr, dt, rows_, V_, stride_ = _logits_desc(logits)
-            st = vlib.ls_sample_verify(ptr, dt, rows_, V_, stride_, D, 1 + S, _dptr(vgather), ctypes.byref(vprm), i,
+            st = vlib.ls_sample_verify(ptr, dt, rows_, V_, stride_, VD, 1 + VS, _dptr(vgather), ctypes.byref(vprm), i,
                                        int(w.no_top_k), int(w.no_top_p), _dptr(cand), _dptr(vtarget), _dptr(vpred),
                                        _dptr(vai), _dptr(van), None, _stream(None))
             assert st == 0, st
@@ -361,9 +362,9 @@ def run_ours(args, world, rank, local):
     peaks, peak_src = measured_peaks()
     alg_bytes = W.algorithmic_bytes(w)
     if args.call == "verify":  # the decode verify rows read once; ids, drafts, predicts, accept outputs
-        D, _, S = w.spec
-        vn = D * (1 + S)
-        alg_bytes = vn * w.vocab * w.elem_bytes + vn * (28 + 4 + 4 + 4 + 4) + D * 4
+        VD, _, VS = w.spec
+        vn = VD * (1 + VS)
+        alg_bytes = vn * w.vocab * w.elem_bytes + vn * (28 + 4 + 4 + 4 + 4) + VD * 4
     elif args.call == "argmax":  # the rows read once, an id written per row (no parameters)
         alg_bytes = w.n * w.vocab * w.elem_bytes + w.n * (4 + (4 if w.gather_indices is not None else 0))
     elif args.call == "fused":  # one read, the log-prob rows written, id + selected log-prob per row
