@@ -90,6 +90,7 @@ struct alignas(16) Shared {
   int cut_bin;
   int min_index;
   int cand_count;
+  unsigned long long step;  // the Philox step word of the call
   int tie_count;        // ties of the maximum met while collecting
   int tie_j[kTieList];  // their vocabulary indices (the first kTieList)
   int glist[kWarps * kWarpList];  // candidate group indices, one slice per warp
@@ -740,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   float* cand_v = gmax + ng_cap;
   int32_t* cand_j = reinterpret_cast<int32_t*>(cand_v + a.cand_cap);
   const int64_t i = blockIdx.x;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel's writes are visible
 
   // ---- row -> (logits row, request) ------------------------------------
   int err = 0;
@@ -840,9 +842,11 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     consume(g0 + STEP, wb);
     issue(g0 + 3 * STEP, wb);
   }
+  // the next kernel on the stream may be scheduled now (it waits for this grid
+  // to complete before it reads memory)
+  asm volatile("griddepcontrol.launch_dependents;");
   // ---- one block reduction: row maximum, total mass, top-k bound --------
   const uint64_t seed = kSample ? a.seed[req] : 0ull;  // its latency overlaps the reduction
-  const uint64_t step = kSample && a.step_ptr ? *a.step_ptr : a.step;
   // Each warp reduces its maximum, rescales every lane's sum to the warp's
   // reference RN(max * c) and adds; after one barrier every warp combines the
   // 16 warp results the same way (fixed order, so S is deterministic and the
@@ -895,6 +899,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     sh.min_index = 0x7FFFFFFF;
     sh.cand_count = 0;
     sh.tie_count = 0;
+    sh.step = kSample && a.step_ptr ? *a.step_ptr : a.step;  // kept in shared memory, read late
   }
   __syncthreads();
   const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
@@ -1088,6 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // winner's score).  Sampling rows that collected candidates recorded their
   // ties there: one thread scores each (sh.best is next read after the cut's
   // barriers); only more than kTieList ties take a pass over the list.
+  const uint64_t step = sh.step;
   const int nties = ties_in_take && lc <= M ? sh.tie_count : -1;
   if (nties >= 0 && nties <= kTieList) {
     if (tid < nties) score_entry(&sh.best, M, T, seed, step, (uint32_t)i, sh.tie_j[tid]);
@@ -1221,7 +1227,20 @@ static ls_status launch_rows(const KernelArgs& a, int32_t n, size_t smem, cudaSt
       return LS_ERR_CUDA;
     if (dev >= 0 && dev < kMaxDevices) opted[dev].store(smem, std::memory_order_relaxed);
   }
-  kern<<<dim3((unsigned)n), dim3(kThreads), smem, stream>>>(a);
+  // Programmatic dependent launch: the grid may be scheduled while the
+  // previous kernel on the stream drains; every CTA waits for that kernel's
+  // completion (griddepcontrol.wait) before it reads any memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return LS_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? LS_OK : LS_ERR_CUDA;
 }
 
