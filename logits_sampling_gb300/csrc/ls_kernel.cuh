@@ -9,14 +9,17 @@
 // maximum and (when the row needs it) the online sum of exp((l - max) / T).
 // Everything after that pass touches only candidate groups -- groups whose
 // maximum clears a provable lower bound of what can be kept or sampled -- and
-// re-reads them from L2:
-//   * exact top-k cut: an adaptive 11-bit radix select on order-preserving keys;
-//   * exact top-p cut: the same select weighted by fixed-point masses
-//     (deterministic 64-bit integer atomics), joint = top-k cut first;
+// re-reads them from L2 once, into a shared-memory candidate list:
+//   * exact top-k cut: an adaptive 11-bit radix select on order-preserving keys
+//     (its first level built while collecting);
+//   * exact top-p cut: the same select weighted by fixed-point masses (32-bit
+//     atomics on (lo, hi) pairs, or per-key counts scaled by the key's weight,
+//     deterministic run to run), joint = top-k cut first;
 //   * Gumbel-max over the kept set with in-register Philox4x32-10 noise, only
-//     for entries within the noise span of the row maximum.
-// The log-probs kernel runs the same selection and then writes the full
-// [vocab] row of log-probs.
+//     for entries within the noise span of the best score of the maximum's ties.
+// The log-probs mode runs the same selection and then writes the full [vocab]
+// row of log-probs; the fused mode does both (and the raw log-prob of the
+// sampled id) from the same pass.
 //
 // The behaviour follows "core.inference.sampling.base" (Sampling.sample_kernel,
 // Sampling.sample_speculative), "core.inference.sampling.flashinfer_sampling"
@@ -966,15 +969,14 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   const bool ties_in_take = kSample && !tie_only;
 
   // ---- collect: candidate groups -> entries >= lc -----------------------
-  // Each warp scans chunks of 128 group maxima (four per lane, one 16-byte
-  // shared load), chunk q going to warp q mod 16, and lists its candidate
-  // groups (maximum >= lc) in its own slice of the group list.  When the
-  // slice could overflow, and at the end, the warp loads the listed groups
-  // (two per lane per round, all loads in flight at once) and takes their
-  // entries >= lc: they are appended to the shared-memory candidate list (one
-  // atomic per warp and round), feed the first select level's histogram and,
-  // when sampling, the maximum's ties are recorded.  No block barrier until
-  // every warp is done.
+  // Each thread tests the maxima of the groups it streamed; a warp prefix
+  // lists the candidate groups (maximum >= lc) in the warp's own slice of the
+  // group list, kWarpList at a time.  The warp loads the listed groups (two
+  // per lane per round for bf16, one for fp32, all loads in flight at once)
+  // and takes their entries >= lc: they are appended to the shared-memory
+  // candidate list (one atomic per warp and round), feed the first select
+  // level's histogram and, when sampling, the maximum's ties are recorded.
+  // No block barrier until every warp is done.
   using RVT = RowView<TIn>;
   int count = 0;
   // Entry >= lc of a loaded group: append it to the list and feed the first
