@@ -197,3 +197,23 @@ def test_speculative_without_gather():
     assert np.array_equal(mp.cpu().numpy(), omap)
     ref = oracle.sample(x, oracle.DTYPE_F32, n, T, k, p, seed, step=3, token_to_request_index=omap)
     check_ids(ids.cpu().numpy(), ref, "spec no gather")
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_largest_vocab(dtype):
+    """A vocabulary at the library's shared-memory limit (one CTA per SM, the
+    smallest candidate list, candidates re-read from L2) and the first size
+    beyond it, which the host rejects."""
+    import logits_sampling_gb300 as ls
+    V = int(ls.max_vocab(ls.LS_DTYPE_BF16 if dtype == W.BF16 else ls.LS_DTYPE_F32))
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((4, V)) * 3).astype(np.float32)
+    x[:, rng.choice(V, 50, replace=False)] += 12.0
+    for (k, p, T) in [(0, 1.0, 1.0), (40, 1.0, 0.7), (0, 0.9, 0.8), (100, 0.95, 1.2)]:
+        _check(_run(x, dtype, T, k, p), f"V={V} {dtype} k={k} p={p}")
+    import torch
+    big = torch.zeros((1, V + 64), dtype=torch.float32 if dtype == W.F32 else torch.bfloat16, device="cuda")
+    prm = ls.SamplingParams.from_host(np.ones(1), np.zeros(1), np.ones(1), np.arange(1))
+    with pytest.raises(ls.LSError) as e:
+        ls.sample(big, 1, prm, 0, False, False)
+    assert e.value.status == 2  # LS_ERR_UNSUPPORTED
