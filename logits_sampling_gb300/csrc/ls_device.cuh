@@ -206,40 +206,8 @@ __device__ __forceinline__ float warp_min(float v) {
   return r;
 }
 
-struct OpMax {
-  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
-};
-struct OpMin {
-  __device__ __forceinline__ float operator()(float a, float b) const { return fminf(a, b); }
-};
 struct OpAddF {
   __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
 };
-struct OpAddU64 {
-  __device__ __forceinline__ unsigned long long operator()(unsigned long long a, unsigned long long b) const {
-    return a + b;
-  }
-};
-struct OpAddI {
-  __device__ __forceinline__ int operator()(int a, int b) const { return a + b; }
-};
-
-// Exclusive prefix sum over threads in threadIdx order.
-__device__ __forceinline__ unsigned long long block_exclusive_scan(unsigned long long v, unsigned long long* red) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  unsigned long long incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  __syncthreads();
-  if (lane == 31) red[w] = incl;
-  __syncthreads();
-  unsigned long long base = 0;
-#pragma unroll
-  for (int i = 0; i < kWarps - 1; ++i) base += i < w ? red[i] : 0ull;  // independent loads
-  return base + incl - v;
-}
 
 }  // namespace lsg
