@@ -100,6 +100,7 @@ struct alignas(16) Shared {
   float red_m[kWarps];
   float red_s[kWarps];
   float red_s2[kWarps];  // raw (T = 1) mass per warp, for the selected log-prob
+  float row_M, row_S, row_S2, row_gamma, row_Lp;  // row scalars from warp 0
 };
 
 // Exact 64-bit add into a (lo, hi) pair of u32 counters with two native
@@ -905,31 +906,56 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     sh.step = kSample && a.step_ptr ? *a.step_ptr : a.step;  // kept in shared memory, read late
   }
   __syncthreads();
-  const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
-  const float M = warp_max(mq);
-  const float gamma = warp_min(lane < kWarps ? sh.red_f[lane] : kPosInf);
+  // warp 0 combines the 16 warp results (fixed order: S is deterministic) and
+  // derives the top-p bound's log; the other warps wait at one more barrier
+  // instead of repeating that work
+  if (tid < 32) {
+    const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
+    const float Mw = warp_max(mq);
+    const float gw = warp_min(lane < kWarps ? sh.red_f[lane] : kPosInf);
+    float Sw = 0.f, S2w = 0.f, Lpw = kNegInf;
+    if (Mw > kNegInf && Mw < kPosInf) {
+      if (need_sum) {
+        const float Rw = __fmul_rn(Mw, c);
+        const float sq = lane < kWarps && mq > kNegInf ? sh.red_s[lane] * ex2(__fmul_rn(mq, c) - Rw) : 0.f;
+        Sw = warp_reduce(sq, OpAddF());
+        // entries below Lp = M + T (ln((1 - p) S / V) - 2) carry less than (1 - p) S e^-2
+        if (p_on && !k_on && Sw <= FLT_MAX) Lpw = Mw + T * (logf((1.f - p) * Sw / (float)V) - 2.f);
+      }
+      if (MODE == MODE_BOTH && want_raw) {
+        const float R2w = __fmul_rn(Mw, kLog2e);
+        const float sq = lane < kWarps && mq > kNegInf ? sh.red_s2[lane] * ex2(__fmul_rn(mq, kLog2e) - R2w) : 0.f;
+        S2w = warp_reduce(sq, OpAddF());
+      }
+    }
+    if (lane == 0) {
+      sh.row_M = Mw;
+      sh.row_S = Sw;
+      sh.row_S2 = S2w;
+      sh.row_gamma = gw;
+      sh.row_Lp = Lpw;
+    }
+  }
+  __syncthreads();
+  const float M = sh.row_M, gamma = sh.row_gamma;
   if (M == kNegInf) {
     row_error(a, i, MODE, LS_ROW_ERR_NO_FINITE);
     return;
   }
   const float R = __fmul_rn(M, c);  // reference exponent of the row (rounded product, never fused)
-  float S = 0.f;
-  if (need_sum && M < kPosInf) {
-    const float sq = lane < kWarps && mq > kNegInf ? sh.red_s[lane] * ex2(__fmul_rn(mq, c) - R) : 0.f;
-    S = warp_reduce(sq, OpAddF());
-  }
+  float S = sh.row_S;
+  float Lp = sh.row_Lp;
   const bool tie_only = greedy || M == kPosInf;  // no temperature-scaled distribution
   // raw mass S2 = sum 2^(v log2 e - R2), R2 = RN(M log2 e) (MODE_BOTH, selected log-prob)
   const float R2 = __fmul_rn(M, kLog2e);
-  float S2 = 0.f;
-  if (MODE == MODE_BOTH && want_raw && M < kPosInf) {
-    const float sq = lane < kWarps && mq > kNegInf ? sh.red_s2[lane] * ex2(__fmul_rn(mq, kLog2e) - R2) : 0.f;
-    S2 = warp_reduce(sq, OpAddF());
-    if (!(S2 <= FLT_MAX)) S2 = total_mass_nan(rv, kLog2e, R2, sh.red_f);
-  }
+  float S2 = sh.row_S2;
+  if (MODE == MODE_BOTH && want_raw && M < kPosInf && !(S2 <= FLT_MAX)) S2 = total_mass_nan(rv, kLog2e, R2, sh.red_f);
 
   // ---- total mass when a NaN entry poisoned the online sum ---------------
-  if (!tie_only && need_sum && !(S <= FLT_MAX)) S = total_mass_nan(rv, c, R, sh.red_f);
+  if (!tie_only && need_sum && !(S <= FLT_MAX)) {
+    S = total_mass_nan(rv, c, R, sh.red_f);
+    if (p_on && !k_on) Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
+  }
 
   // ---- candidate bound --------------------------------------------------
   // Every entry that a later phase needs is >= lc:
@@ -948,7 +974,6 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     lc = gamma > kNegInf ? gamma : -FLT_MAX;
     kind = 1;
   } else if (p_on) {
-    const float Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
     lc = fminf(fmaxf(Lp, -FLT_MAX), M);
     kind = 2;
   } else {
