@@ -89,6 +89,7 @@ struct alignas(16) Shared {
   unsigned long long best;
   unsigned int acc[2];  // a count in acc[0], or a mass as a (lo, hi) pair
   unsigned long long cut_above;
+  unsigned long long cut_total, cut_target;  // level total and (joint) target, from thread 0
   unsigned long long cut_mass;
   int cut_bin;
   int min_index;
@@ -587,45 +588,56 @@ __device__ __forceinline__ unsigned long long find_cut_bin(Shared& sh, int nb, u
                                                            const W& weight) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int top = nb - 1 - t * kBinsPerThread;
-  unsigned long long w[kBinsPerThread], local = 0;
+  // warps holding no bin only write a zero total and meet the barriers
+  const bool has_bins = nb - 1 - warp * 32 * kBinsPerThread >= 0;
+  unsigned long long w[kBinsPerThread], local = 0, incl = 0;
+  if (has_bins) {
 #pragma unroll
-  for (int q = 0; q < kBinsPerThread; ++q) {
-    w[q] = top - q >= 0 ? weight(top - q) : 0ull;
-    local += w[q];
-  }
-  unsigned long long incl = local;
+    for (int q = 0; q < kBinsPerThread; ++q) {
+      w[q] = top - q >= 0 ? weight(top - q) : 0ull;
+      local += w[q];
+    }
+    incl = local;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += u;
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += u;
+    }
   }
   if (t == 0) sh.cut_bin = -1;
   if (lane == 31) sh.red_u64[warp] = incl;
   __syncthreads();
-  unsigned long long base = 0, total = 0;
+  if (has_bins) {
+    unsigned long long base = 0, total = 0;
 #pragma unroll
-  for (int i = 0; i < kWarps; ++i) {
-    const unsigned long long x = sh.red_u64[i];
-    base += i < warp ? x : 0ull;
-    total += x;
-  }
-  if (joint_p >= 0.f) target = __float2ull_ru(joint_p * __ull2float_rn(total));
-  if (target < 1ull) target = 1ull;
-  unsigned long long cum = above + base + incl - local;
-  if (cum < target && cum + local >= target) {
+    for (int i = 0; i < kWarps; ++i) {
+      const unsigned long long x = sh.red_u64[i];
+      base += i < warp ? x : 0ull;
+      total += x;
+    }
+    if (joint_p >= 0.f) target = __float2ull_ru(joint_p * __ull2float_rn(total));
+    if (target < 1ull) target = 1ull;
+    if (t == 0) {
+      sh.cut_total = total;
+      sh.cut_target = target;
+    }
+    unsigned long long cum = above + base + incl - local;
+    if (cum < target && cum + local >= target) {
 #pragma unroll
-    for (int q = 0; q < kBinsPerThread; ++q) {
-      if (cum + w[q] >= target) {
-        sh.cut_bin = top - q;
-        sh.cut_above = cum;
-        sh.cut_mass = w[q];
-        break;
+      for (int q = 0; q < kBinsPerThread; ++q) {
+        if (cum + w[q] >= target) {
+          sh.cut_bin = top - q;
+          sh.cut_above = cum;
+          sh.cut_mass = w[q];
+          break;
+        }
+        cum += w[q];
       }
-      cum += w[q];
     }
   }
   __syncthreads();
-  return total;
+  target = sh.cut_target;  // the same in every thread (set by warp 0, which always holds bins)
+  return sh.cut_total;
 }
 
 struct SelResult {
