@@ -70,6 +70,9 @@ struct KernelArgs {
 
 constexpr int kWarpList = 128;  // candidate groups a warp lists before loading them
 constexpr int kTieList = 32;    // ties of the maximum recorded while collecting
+// Slack of the top-p candidate bound: the entries below it carry at most
+// e^-kTopPSlack of the mass that the cut leaves out.
+constexpr float kTopPSlack = 0.25f;
 
 // Group-maximum slots of a row: worst-case row alignment, rounded up to whole
 // 16-byte vectors (the candidate list that follows stays 16-byte aligned).
@@ -643,6 +646,7 @@ __device__ __forceinline__ unsigned long long find_cut_bin(Shared& sh, int nb, u
 struct SelResult {
   uint32_t key;                 // kept set: entries with key >= this
   unsigned long long mass_ge;   // weight of the kept entries
+  bool short_total;             // the whole range weighs less than the target
 };
 
 // Exact threshold select over the row entries with keys in [klo, khi], given
@@ -690,7 +694,7 @@ __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo
         find_cut_bin(sh, nb, above, target, joint_p, BinWeight<TIn>{&sh, mode, klo, c, R});
     joint_p = -1.f;
     const int b = sh.cut_bin;
-    if (b < 0) return SelResult{klo, above + total};  // only reachable on the first level
+    if (b < 0) return SelResult{klo, above + total, true};  // only reachable on the first level
     above = sh.cut_above;
     mass_at = sh.cut_mass;
     const uint32_t nlo = klo + ((uint32_t)b << shift);
@@ -700,7 +704,7 @@ __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo
     if (klo >= khi) break;  // a single key left
     __syncthreads();        // the cut fields and the histogram are rewritten by the next level
   }
-  return SelResult{klo, above + mass_at};
+  return SelResult{klo, above + mass_at, false};
 }
 
 __device__ __forceinline__ void row_error(const KernelArgs& a, int64_t i, int mode, int err) {
@@ -931,8 +935,8 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
         const float Rw = __fmul_rn(Mw, c);
         const float sq = lane < kWarps && mq > kNegInf ? sh.red_s[lane] * ex2(__fmul_rn(mq, c) - Rw) : 0.f;
         Sw = warp_reduce(sq, OpAddF());
-        // entries below Lp = M + T (ln((1 - p) S / V) - 2) carry less than (1 - p) S e^-2
-        if (p_on && !k_on && Sw <= FLT_MAX) Lpw = Mw + T * (logf((1.f - p) * Sw / (float)V) - 2.f);
+        // entries below Lp = M + T (ln((1 - p) S / V) - slack) carry less than (1 - p) S e^-slack
+        if (p_on && !k_on && Sw <= FLT_MAX) Lpw = Mw + T * (logf((1.f - p) * Sw / (float)V) - kTopPSlack);
       }
       if (MODE == MODE_BOTH && want_raw) {
         const float R2w = __fmul_rn(Mw, kLog2e);
@@ -966,15 +970,16 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // ---- total mass when a NaN entry poisoned the online sum ---------------
   if (!tie_only && need_sum && !(S <= FLT_MAX)) {
     S = total_mass_nan(rv, c, R, sh.red_f);
-    if (p_on && !k_on) Lp = M + T * (logf((1.f - p) * S / (float)V) - 2.f);
+    if (p_on && !k_on) Lp = M + T * (logf((1.f - p) * S / (float)V) - kTopPSlack);
   }
 
   // ---- candidate bound --------------------------------------------------
   // Every entry that a later phase needs is >= lc:
   //  * ties-only rows (greedy, +inf maximum): the maximum itself;
   //  * top-k: gamma (at least k entries are >= gamma);
-  //  * top-p alone: the entries below Lp carry less than (1 - p) S e^-2, so
-  //    the cut lies above Lp;
+  //  * top-p alone: the entries below Lp carry less than (1 - p) S e^-slack,
+  //    so the cut lies above Lp (if rounding of S, or of Lp for a tiny T and
+  //    large logits, ever beat the slack, the cut detects it: see there);
   //  * no filter: an entry with z more than the noise span below max z can
   //    never beat the maximum's perturbed score.
   const float lg = M - kGumbelSpan * T;
@@ -1125,7 +1130,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     __syncthreads();
     count = sh.cand_count;
   }
-  const Cands<TIn> cs{&rv, gmax, cand_v, cand_j, count, lc <= M && count <= a.cand_cap};
+  Cands<TIn> cs{&rv, gmax, cand_v, cand_j, count, lc <= M && count <= a.cand_cap};
 
   // The maximum's ties: lowest index (greedy), count (log-probs of ties-only
   // rows) or exact Gumbel score (sampling; the best is a lower bound of the
@@ -1178,7 +1183,15 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     // the first level's histogram was built while collecting
     const unsigned long long target =
         kind == 1 ? (unsigned long long)k : max(1ull, __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale));
-    const SelResult r1 = radix_select<TIn>(sh, cs, klo1, key_max, target, -1.f, R, c, 0ull, kind == 2, true);
+    SelResult r1 = radix_select<TIn>(sh, cs, klo1, key_max, target, -1.f, R, c, 0ull, kind == 2, true);
+    if (kind == 2 && r1.short_total && lc > -FLT_MAX) {
+      // The candidates weigh less than the top-p target, so the cut lies
+      // below the bound: select again over every finite entry, visiting the
+      // groups from global memory (the list holds only entries >= lc).  The
+      // maximum's ties are all candidates, so their scores stand.
+      cs.listed = false;
+      r1 = radix_select<TIn>(sh, cs, K::key(-FLT_MAX), key_max, target, -1.f, R, c, 0ull, true, false);
+    }
     lo_key = r1.key;
     kept_mass = r1.mass_ge;
   }
