@@ -1135,12 +1135,15 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // The maximum's ties: lowest index (greedy), count (log-probs of ties-only
   // rows) or exact Gumbel score (sampling; the best is a lower bound of the
   // winner's score).  Sampling rows that collected candidates recorded their
-  // ties there: one thread scores each (sh.best is next read after the cut's
-  // barriers); only more than kTieList ties take a pass over the list.
+  // ties there: one thread of the last warps scores each (those warps hold no
+  // bin of a small first select level, whose scan leads warp 0; sh.best is
+  // next read after the cut's barriers); only more than kTieList ties take a
+  // pass over the list.
   const uint64_t step = sh.step;
   const int nties = ties_in_take && lc <= M ? sh.tie_count : -1;
   if (nties >= 0 && nties <= kTieList) {
-    if (tid < nties) score_entry(&sh.best, M, T, seed, step, (uint32_t)i, sh.tie_j[tid]);
+    const int q = kThreads - 1 - tid;
+    if (q < nties) score_entry(&sh.best, M, T, seed, step, (uint32_t)i, sh.tie_j[q]);
   } else if (tie_only || kSample) {
     cs.each(M, [&](float x, int64_t j) {
       if (MODE != MODE_SAMPLE && tie_only) atomicAdd(&sh.acc[0], 1u);
