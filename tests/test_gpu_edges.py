@@ -128,6 +128,17 @@ def test_degenerate_filters(dtype):
             assert np.all(out[0] == 100)
 
 
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_top_p_near_one(dtype):
+    # p just under the point where the filter switches off: the kept set is
+    # most of a wide row, the candidate bound sits deep in the tail and the
+    # candidates overflow the shared-memory list
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((6, 50000)) * np.array([1, 1, 3, 3, 0.2, 6], np.float32)[:, None]).astype(np.float32)
+    for (p, T) in [(0.99, 1.0), (0.9999, 0.7), (0.99998, 1.5), (0.99998, 0.3)]:
+        _check(_run(x, dtype, T, 0, p), f"near one {dtype} p={p} T={T}")
+
+
 def test_ties_at_the_cut():
     x = np.tile(np.array([5, 5, 5, 3, 3, 3, 3, 1, 1, 0], np.float32), (4, 1))
     for (k, p) in [(2, 1.0), (4, 1.0), (0, 0.3), (0, 0.97), (5, 0.5)]:
