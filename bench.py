@@ -164,12 +164,13 @@ def to_device(w, device):
     return torch.from_numpy(w.logits).to(device)
 
 
-def cpu_oracle_rate(w, target_s=8.0, max_rows=None):
-    """Time the CPU oracle on a bounded sample of the workload's rows; returns
+def cpu_oracle_rate(w, target_s=8.0, max_rows=None, threads=None):
+    """Time the CPU oracle on a bounded sample of the workload's rows (on all
+    the host cores this process may use, or on `threads` of them); returns
     (rows/s, seconds, rows, threads)."""
     import oracle
     from logits_sampling_gb300 import workloads as W
-    threads = oracle.default_threads()
+    threads = oracle.default_threads() if threads is None else threads
     odt = oracle.DTYPE_BF16 if w.dtype == W.BF16 else oracle.DTYPE_F32
     mapping = oracle.speculative_mapping(*w.spec) if w.spec is not None else w.token_to_request_index
     rows = w.n if max_rows is None else min(w.n, max_rows)
@@ -395,6 +396,11 @@ def run_ours(args, world, rank, local):
         line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{done} rows ({min(w.n, args.ref_rows)} of the workload's {w.n} per "
                                           f"pass) in {el:.1f} s"}
+        # the same oracle on one core, on a smaller sample
+        rows1 = min(w.n, 8)
+        rate1, el1, done1, _ = cpu_oracle_rate(w, target_s=min(3.0, args.cpu_s), max_rows=rows1, threads=1)
+        line["cpu_baseline"]["single_core"] = {"value": rate1, "unit": "rows/s", "cores": 1,
+                                               "sample": f"{done1} rows ({rows1} per pass) in {el1:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
