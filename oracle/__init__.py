@@ -49,10 +49,10 @@ def _load():
         lib.oracle_speculative_mapping.argtypes = [i32, i32, i32, P]
         lib.oracle_speculative_mapping.restype = None
         lib.oracle_sample.argtypes = [P, ctypes.c_int, i64, i64, i64, i32, P, P, P, P, P, P, i32, u64,
-                                      ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, ctypes.c_int]
+                                      ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P, ctypes.c_int]
         lib.oracle_sample.restype = ctypes.c_int
-        lib.oracle_log_probs.argtypes = [P, ctypes.c_int, i64, i64, i64, i32, P, P, P, P, P, i32, P, P, P, P,
-                                         ctypes.c_int]
+        lib.oracle_log_probs.argtypes = [P, ctypes.c_int, i64, i64, i64, i32, P, P, P, P, P, i32, P, P, P, P, P,
+                                         P, ctypes.c_int]
         lib.oracle_log_probs.restype = ctypes.c_int
         lib.oracle_selected_log_probs.argtypes = [P, ctypes.c_int, i64, i64, i64, i32, P, P, P]
         lib.oracle_selected_log_probs.restype = ctypes.c_int
@@ -119,6 +119,9 @@ def sample(logits, dtype, n, temperature, top_k, top_p, seed, step=0, no_top_k=F
            gather_indices=None, token_to_request_index=None, vocab=None, want_kept=True, want_lp=False,
            nthreads=None):
     """Reference sampling.  Returns a dict with ids [n], kept [n, V] (bool),
+    kept_loose / kept_tight [n, V] (bool, with want_kept: for a row flagged as
+    a top-p near-tie, the kept sets at the lowest and the highest cut that a
+    target within the 1e-5 band gives; the kept set on every other row),
     lp [n, V] (float64, optional), flags [n], top2 [n, 2], error_word."""
     a = _logits_args(logits, dtype)
     rows, stride = a.shape
@@ -133,23 +136,28 @@ def sample(logits, dtype, n, temperature, top_k, top_p, seed, step=0, no_top_k=F
     t = None if token_to_request_index is None else np.ascontiguousarray(token_to_request_index, dtype=np.int32)
     ids = np.zeros(n, dtype=np.int32)
     kept = np.zeros((n, V), dtype=np.uint8) if want_kept else None
+    kept_loose = np.zeros((n, V), dtype=np.uint8) if want_kept else None
+    kept_tight = np.zeros((n, V), dtype=np.uint8) if want_kept else None
     lp = np.zeros((n, V), dtype=np.float64) if want_lp else None
     flags = np.zeros(n, dtype=np.int32)
     top2 = np.zeros((n, 2), dtype=np.float64)
     err = np.zeros(1, dtype=np.int32)
     rc = _load().oracle_sample(_ptr(a), dtype, rows, V, stride, n, _ptr(g), _ptr(t), _ptr(temperature),
                                _ptr(top_k), _ptr(top_p), _ptr(seed), nreq, int(step), int(bool(no_top_k)),
-                               int(bool(no_top_p)), _ptr(ids), _ptr(kept), _ptr(lp), _ptr(flags), _ptr(top2),
-                               _ptr(err), int(nthreads or default_threads()))
+                               int(bool(no_top_p)), _ptr(ids), _ptr(kept), _ptr(kept_loose), _ptr(kept_tight),
+                               _ptr(lp), _ptr(flags), _ptr(top2), _ptr(err), int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle_sample failed ({rc})")
-    return {"ids": ids, "kept": None if kept is None else kept.astype(bool), "lp": lp, "flags": flags,
+    return {"ids": ids, "kept": None if kept is None else kept.astype(bool),
+            "kept_loose": None if kept_loose is None else kept_loose.astype(bool),
+            "kept_tight": None if kept_tight is None else kept_tight.astype(bool), "lp": lp, "flags": flags,
             "top2": top2, "error_word": int(err[0])}
 
 
 def log_probs(logits, dtype, num_rows, temperature, top_k, top_p, gather_indices=None,
               token_to_request_index=None, vocab=None, nthreads=None):
-    """Reference log-probs [num_rows, V] (float64) of the processed distribution."""
+    """Reference log-probs [num_rows, V] (float64) of the processed distribution,
+    with kept, kept_loose, kept_tight (as for sample), flags and error_word."""
     a = _logits_args(logits, dtype)
     rows, stride = a.shape
     V = stride if vocab is None else vocab
@@ -161,14 +169,18 @@ def log_probs(logits, dtype, num_rows, temperature, top_k, top_p, gather_indices
     t = None if token_to_request_index is None else np.ascontiguousarray(token_to_request_index, dtype=np.int32)
     lp = np.zeros((num_rows, V), dtype=np.float64)
     kept = np.zeros((num_rows, V), dtype=np.uint8)
+    kept_loose = np.zeros((num_rows, V), dtype=np.uint8)
+    kept_tight = np.zeros((num_rows, V), dtype=np.uint8)
     flags = np.zeros(num_rows, dtype=np.int32)
     err = np.zeros(1, dtype=np.int32)
     rc = _load().oracle_log_probs(_ptr(a), dtype, rows, V, stride, num_rows, _ptr(g), _ptr(t),
                                   _ptr(temperature), _ptr(top_k), _ptr(top_p), nreq, _ptr(lp), _ptr(kept),
-                                  _ptr(flags), _ptr(err), int(nthreads or default_threads()))
+                                  _ptr(kept_loose), _ptr(kept_tight), _ptr(flags), _ptr(err),
+                                  int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle_log_probs failed ({rc})")
-    return {"lp": lp, "kept": kept.astype(bool), "flags": flags, "error_word": int(err[0])}
+    return {"lp": lp, "kept": kept.astype(bool), "kept_loose": kept_loose.astype(bool),
+            "kept_tight": kept_tight.astype(bool), "flags": flags, "error_word": int(err[0])}
 
 
 def selected_log_probs(logits, dtype, ids, gather_indices=None, vocab=None):

@@ -177,6 +177,8 @@ typedef struct {
   /* outputs (nullable except ids when sampling) */
   int32_t* out_ids;
   uint8_t* out_kept;
+  uint8_t* out_kept_loose; /* flagged top-p rows: kept set at the lowest cut the band allows */
+  uint8_t* out_kept_tight; /* flagged top-p rows: kept set at the highest cut the band allows */
   double* out_lp;
   int32_t* out_flags;
   double* out_top2;
@@ -189,6 +191,8 @@ static void fill_error_row(const oracle_job* jb, int64_t i) {
   const int64_t V = jb->vocab;
   if (jb->out_ids) jb->out_ids[i] = -1;
   if (jb->out_kept) memset(jb->out_kept + i * V, 0, (size_t)V);
+  if (jb->out_kept_loose) memset(jb->out_kept_loose + i * V, 0, (size_t)V);
+  if (jb->out_kept_tight) memset(jb->out_kept_tight + i * V, 0, (size_t)V);
   if (jb->out_lp)
     for (int64_t j = 0; j < V; ++j) jb->out_lp[i * V + j] = NAN;
 }
@@ -233,6 +237,7 @@ static void process_row(const oracle_job* jb, int64_t i, double* l, double* z, u
 
   int32_t id = -1;
   int32_t flags = 0;
+  int topp_cut = 0; /* set when step 6 wrote out_kept_loose / out_kept_tight */
   if (greedy) {
     /* 3. greedy: the maximum's ties, lowest index sampled */
     int64_t cnt = 0;
@@ -262,6 +267,7 @@ static void process_row(const oracle_job* jb, int64_t i, double* l, double* z, u
     /* 6. top-p over the (top-k restricted) distribution */
     float p = jb->top_p[req];
     if (jb->allow_top_p && p < 0.99999f) {
+      topp_cut = 1;
       double zmax = -INFINITY;
       for (int64_t j = 0; j < V; ++j)
         if (kept[j] && z[j] > zmax) zmax = z[j];
@@ -276,7 +282,13 @@ static void process_row(const oracle_job* jb, int64_t i, double* l, double* z, u
         }
       qsort(sorted, (size_t)m, sizeof(oracle_vj), cmp_vj_desc);
       double target = (double)p * total;
-      double cum = 0.0, cut = sorted[0].v;
+      /* The exemption band: a sampler whose target differs from this one by
+       * at most 1e-5 * total may place the cut anywhere from the first value
+       * whose cumulative mass reaches target - band (tight) down to the first
+       * that reaches target + band (loose).  The walk continues past the cut
+       * to find the loose value. */
+      const double band = 1e-5 * total;
+      double cum = 0.0, cut = NAN, tight = NAN, loose = NAN;
       int64_t a = 0;
       while (a < m) { /* walk groups of equal z */
         int64_t b = a;
@@ -284,15 +296,26 @@ static void process_row(const oracle_job* jb, int64_t i, double* l, double* z, u
         while (b < m && sorted[b].v == sorted[a].v) mass += exp(sorted[b++].v - zmax);
         double before = cum;
         cum += mass;
-        if (cum >= target) {
+        if (isnan(tight) && cum >= target - band) tight = sorted[a].v;
+        if (isnan(cut) && cum >= target) {
           cut = sorted[a].v;
-          if (fabs(cum - target) <= 1e-5 * total || (a > 0 && fabs(before - target) <= 1e-5 * total))
+          if (fabs(cum - target) <= band || (a > 0 && fabs(before - target) <= band))
             flags |= ORACLE_FLAG_TOP_P_TIE;
+        }
+        if (!isnan(cut) && cum >= target + band) {
+          loose = sorted[a].v;
           break;
         }
         a = b;
       }
-      if (a >= m) cut = sorted[m - 1].v; /* unreachable in exact arithmetic */
+      if (isnan(cut)) cut = sorted[m - 1].v; /* unreachable in exact arithmetic */
+      if (isnan(tight)) tight = cut;
+      if (isnan(loose)) loose = sorted[m - 1].v;
+      if (!(flags & ORACLE_FLAG_TOP_P_TIE)) tight = loose = cut;
+      if (jb->out_kept_loose)
+        for (int64_t j = 0; j < V; ++j) jb->out_kept_loose[i * V + j] = kept[j] && (z[j] >= loose);
+      if (jb->out_kept_tight)
+        for (int64_t j = 0; j < V; ++j) jb->out_kept_tight[i * V + j] = kept[j] && (z[j] >= tight);
       for (int64_t j = 0; j < V; ++j) kept[j] = kept[j] && (z[j] >= cut);
     }
     /* 8. log-probs of the processed distribution */
@@ -331,6 +354,8 @@ static void process_row(const oracle_job* jb, int64_t i, double* l, double* z, u
   jb->row_error[i] = 0;
   if (jb->out_ids) jb->out_ids[i] = id;
   if (jb->out_kept) memcpy(jb->out_kept + i * V, kept, (size_t)V);
+  if (jb->out_kept_loose && !topp_cut) memcpy(jb->out_kept_loose + i * V, kept, (size_t)V);
+  if (jb->out_kept_tight && !topp_cut) memcpy(jb->out_kept_tight + i * V, kept, (size_t)V);
   if (jb->out_flags) jb->out_flags[i] = flags;
 }
 
@@ -401,12 +426,16 @@ static int run_job(oracle_job* base, int32_t* error_word) {
 }
 
 /* Sample n rows.  All pointers are host memory.  out_kept (n*V bytes),
+ * out_kept_loose and out_kept_tight (n*V bytes each: for a row flagged as a
+ * top-p near-tie, the kept sets at the lowest and the highest cut that a
+ * target within the 1e-5 band gives; the kept set on every other row),
  * out_lp (n*V doubles), out_flags (n) and out_top2 (2n) may be NULL. */
 int oracle_sample(const void* logits, int dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride, int32_t n,
                   const int32_t* gather, const int32_t* t2r, const float* temperature, const int32_t* top_k,
                   const float* top_p, const uint64_t* seed, int32_t num_requests, uint64_t step, int no_top_k,
-                  int no_top_p, int32_t* out_ids, uint8_t* out_kept, double* out_lp, int32_t* out_flags,
-                  double* out_top2, int32_t* error_word, int nthreads) {
+                  int no_top_p, int32_t* out_ids, uint8_t* out_kept, uint8_t* out_kept_loose,
+                  uint8_t* out_kept_tight, double* out_lp, int32_t* out_flags, double* out_top2,
+                  int32_t* error_word, int nthreads) {
   oracle_job jb;
   memset(&jb, 0, sizeof jb);
   jb.logits = logits;
@@ -428,6 +457,8 @@ int oracle_sample(const void* logits, int dtype, int64_t logits_rows, int64_t vo
   jb.want_sample = 1;
   jb.out_ids = out_ids;
   jb.out_kept = out_kept;
+  jb.out_kept_loose = out_kept_loose;
+  jb.out_kept_tight = out_kept_tight;
   jb.out_lp = out_lp;
   jb.out_flags = out_flags;
   jb.out_top2 = out_top2;
@@ -506,11 +537,14 @@ void oracle_verify_chain(const int32_t* candidates, const int32_t* target_sample
 }
 
 /* Log-probs of the processed distribution for num_rows rows (every row's own
- * top-k and top-p apply; there are no batch route flags on this call). */
+ * top-k and top-p apply; there are no batch route flags on this call).
+ * out_kept, out_kept_loose and out_kept_tight (n*V bytes each, nullable) as
+ * for oracle_sample. */
 int oracle_log_probs(const void* logits, int dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
                      int32_t num_rows, const int32_t* gather, const int32_t* t2r, const float* temperature,
                      const int32_t* top_k, const float* top_p, int32_t num_requests, double* out_lp,
-                     uint8_t* out_kept, int32_t* out_flags, int32_t* error_word, int nthreads) {
+                     uint8_t* out_kept, uint8_t* out_kept_loose, uint8_t* out_kept_tight, int32_t* out_flags,
+                     int32_t* error_word, int nthreads) {
   oracle_job jb;
   memset(&jb, 0, sizeof jb);
   jb.logits = logits;
@@ -530,6 +564,8 @@ int oracle_log_probs(const void* logits, int dtype, int64_t logits_rows, int64_t
   jb.want_sample = 0;
   jb.out_lp = out_lp;
   jb.out_kept = out_kept;
+  jb.out_kept_loose = out_kept_loose;
+  jb.out_kept_tight = out_kept_tight;
   jb.out_flags = out_flags;
   jb.nthreads = nthreads;
   return run_job(&jb, error_word);

@@ -7,11 +7,9 @@ import pytest
 import oracle
 from logits_sampling_gb300 import workloads as W
 
-from gpu_util import check_ids, check_log_probs, odt, params_of, to_device
+from gpu_util import check_ids, check_log_probs, odt, params_of, selected_tolerance, to_device
 
 pytestmark = pytest.mark.gpu
-
-SEL_ATOL = 1e-4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,14 +51,14 @@ def _check(w, out, route=None, step=None, gather=None, t2r=None, where=""):
     assert err == ref["error_word"], (where, err, ref["error_word"])
     check_ids(ids, ref, where)
     if lp is not None:
-        check_log_probs(lp, ref["lp"], ref["kept"], ref["flags"], where + " lp")
+        check_log_probs(lp, ref, where + " lp")
     if sel is not None:
         want = oracle.selected_log_probs(w.logits, odt(w), np.where(ids >= 0, ids, 0), gather_indices=gather)
         for i in range(n):
             if ids[i] < 0:
                 assert np.isnan(sel[i]), (where, i)
                 continue
-            tol = max(SEL_ATOL, 2.0 * float(np.spacing(np.float32(abs(want[i])))))
+            tol = float(selected_tolerance(want[i]))
             assert abs(float(sel[i]) - want[i]) <= tol or (np.isinf(want[i]) and sel[i] == want[i]), \
                 (where, i, float(sel[i]), want[i])
 

@@ -49,7 +49,7 @@ def test_tiny_ids_and_log_probs():
     r, g, t, n = _lp_oracle(w)
     lp, err = gpu_log_probs(w, gather=g, t2r=t, num_rows=n)
     assert err == 0
-    check_log_probs(lp, r["lp"], r["kept"], r["flags"], "tiny lp")
+    check_log_probs(lp, r, "tiny lp")
 
 
 def test_decode_ids_and_log_probs():
@@ -59,7 +59,7 @@ def test_decode_ids_and_log_probs():
     check_ids(ids, oracle_sample(w), "decode")
     r, g, t, n = _lp_oracle(w)
     lp, _ = gpu_log_probs(w, gather=g, t2r=t, num_rows=n)
-    check_log_probs(lp, r["lp"], r["kept"], r["flags"], "decode lp")
+    check_log_probs(lp, r, "decode lp")
 
 
 def test_top_p_full_size_ids():
@@ -73,7 +73,7 @@ def test_top_p_log_probs_sampled_rows():
     w = W.make_top_p(rows=24)
     r, g, t, n = _lp_oracle(w)
     lp, _ = gpu_log_probs(w, gather=g, t2r=t, num_rows=n)
-    check_log_probs(lp, r["lp"], r["kept"], r["flags"], "top_p lp")
+    check_log_probs(lp, r, "top_p lp")
 
 
 def test_speculative_full_size_ids_and_mapping():
@@ -90,7 +90,7 @@ def test_speculative_log_probs_sampled_rows():
     r, g, t, n = _lp_oracle(w, rows)
     x = to_device(w)
     lp, _ = gpu_log_probs(w, logits_dev=x, gather=g, t2r=t, num_rows=n)
-    check_log_probs(lp, r["lp"], r["kept"], r["flags"], "speculative lp")
+    check_log_probs(lp, r, "speculative lp")
 
 
 def test_large_full_size_ids():
@@ -105,7 +105,7 @@ def test_large_log_probs_sampled_rows():
     w = W.make_large(rows=64, vocab=262144)
     r, g, t, n = _lp_oracle(w)
     lp, _ = gpu_log_probs(w, gather=g, t2r=t, num_rows=n)
-    check_log_probs(lp, r["lp"], r["kept"], r["flags"], "large lp")
+    check_log_probs(lp, r, "large lp")
 
 
 # ---------------------------------------------------------------------------

@@ -484,6 +484,54 @@ def test_top_p_tie_flag():
     assert not (_sample(clear, 1.0, 0, 0.5)["flags"][0] & oracle.FLAG_TOP_P_TIE)
 
 
+def test_top_p_tie_band_kept_sets():
+    """Closed forms.  Logits (1, 0, -1, -2) at T = 1 weigh 1, e^-1, e^-2, e^-3
+    relative to the maximum.  With p = 1 / S the first value alone carries the
+    target mass, so the row is flagged, the kept set is {0}, the tight set (a
+    target 1e-5 S lower) {0} and the loose set (a target 1e-5 S higher) {0, 1}.
+    Under top_k = 2 the loose set stays inside the top-k set.  A deep tail of
+    many tiny, distinct masses puts several values inside the band: the loose
+    set then reaches past the next value.  Unflagged rows: tight = loose = kept."""
+    def below(x):  # the largest float32 not above x: p * S stays at or below the first value's mass
+        f = np.float32(x)
+        return f if float(f) <= x else np.nextafter(f, np.float32(0))
+
+    row = np.array([[1.0, 0.0, -1.0, -2.0]], np.float32)
+    S = 1.0 + math.exp(-1) + math.exp(-2) + math.exp(-3)
+    r = _sample(row, 1.0, 0, below(1.0 / S))
+    assert r["flags"][0] & oracle.FLAG_TOP_P_TIE
+    assert list(np.nonzero(r["kept"][0])[0]) == [0]
+    assert list(np.nonzero(r["kept_tight"][0])[0]) == [0]
+    assert list(np.nonzero(r["kept_loose"][0])[0]) == [0, 1]
+    lp = oracle.log_probs(row, F32, 1, np.float32([1.0]), np.int32([0]), np.float32([below(1.0 / S)]))
+    for key in ("kept", "kept_loose", "kept_tight"):
+        assert np.array_equal(lp[key], r[key]), key
+    rk = _sample(row, 1.0, 2, below(1.0 / (1.0 + math.exp(-1))))
+    assert rk["flags"][0] & oracle.FLAG_TOP_P_TIE
+    assert list(np.nonzero(rk["kept"][0])[0]) == [0]
+    assert list(np.nonzero(rk["kept_loose"][0])[0]) == [0, 1]
+    # value 0 carries mass 1; fifty distinct tail values near ln(2e-6) carry
+    # about 2e-6 each (1e-4 together).  With the target inside the tail
+    # (p = 1 - 5e-5) the band of +-1e-5 S spans about five tail values on
+    # each side of the cut: tight < kept < loose by several values each
+    tail = np.array([0.0] + [math.log(2e-6) - 0.001 * t for t in range(50)], np.float32)[None, :]
+    rt = _sample(tail, 1.0, 0, np.float32(1.0 - 5e-5))
+    kt, kc, kl = (int(rt[key][0].sum()) for key in ("kept_tight", "kept", "kept_loose"))
+    assert rt["flags"][0] & oracle.FLAG_TOP_P_TIE
+    assert np.all(rt["kept_tight"][0] <= rt["kept"][0]) and np.all(rt["kept"][0] <= rt["kept_loose"][0])
+    assert kt + 3 <= kc <= kl - 3, (kt, kc, kl)
+    clear = _sample(np.array([[3.0, 0.0, -5.0, 1.0]], np.float32), 1.0, 0, 0.5)
+    assert clear["flags"][0] == 0
+    assert np.array_equal(clear["kept_loose"], clear["kept"]) and np.array_equal(clear["kept_tight"], clear["kept"])
+    rng = np.random.default_rng(3)
+    many = _sample((rng.standard_normal((64, 40)) * 2).astype(np.float32), 0.9, 5, 0.8)
+    for i in range(64):
+        if not many["flags"][i] & oracle.FLAG_TOP_P_TIE:
+            assert np.array_equal(many["kept_loose"][i], many["kept"][i])
+            assert np.array_equal(many["kept_tight"][i], many["kept"][i])
+        assert np.all(many["kept_loose"][i] >= many["kept"][i]) and np.all(many["kept"][i] >= many["kept_tight"][i])
+
+
 # --------------------------------------------------------------------------
 # selected-token log-prob under the raw logits
 # --------------------------------------------------------------------------
