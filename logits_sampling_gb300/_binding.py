@@ -153,19 +153,32 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _on(stream):
+    """The stream a call runs on (the current stream when None) and a context
+    that makes it current: outputs and temporaries are allocated and filled on
+    the stream the kernels use, so an explicit stream never races with the
+    call's own set-up, and the caching allocator reuses their memory only in
+    that stream's order."""
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s, torch.cuda.stream(s)
+
+
 def sample(logits, n, params, step, no_top_k, no_top_p, gather_indices=None, token_to_request_index=None,
            out=None, error_word=None, stream=None):
     """ls_sample: returns out (int32 [n] on the logits' device)."""
     import torch
     lib = load_library()
     ptr, dt, rows, V, stride = _logits_desc(logits)
-    if out is None:
-        out = torch.empty(n, dtype=torch.int32, device=logits.device)
-    prm = params.as_struct()
-    st = lib.ls_sample(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
-                       _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm), int(step),
-                       int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"), _i32(error_word, "error_word"),
-                       _stream(stream))
+    s, ctx = _on(stream)
+    with ctx:
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device=logits.device)
+        prm = params.as_struct()
+        st = lib.ls_sample(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
+                           _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm), int(step),
+                           int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"),
+                           _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_sample")
     return out
@@ -179,14 +192,17 @@ def sample_speculative(required_logits, num_decode, num_prefill, num_speculative
     lib = load_library()
     ptr, dt, rows, V, stride = _logits_desc(required_logits)
     n = num_decode * (1 + num_speculative_tokens) + num_prefill
-    if out is None:
-        out = torch.empty(n, dtype=torch.int32, device=required_logits.device)
-    prm = params.as_struct()
-    st = lib.ls_sample_speculative(ptr, dt, rows, V, stride, int(num_decode), int(num_prefill),
-                                   int(num_speculative_tokens), _i32(gather_indices, "gather_indices"),
-                                   ctypes.byref(prm), int(step), int(bool(no_top_k)), int(bool(no_top_p)),
-                                   _i32(out, "out"), _i32(out_token_to_request_index, "out_token_to_request_index"),
-                                   _i32(error_word, "error_word"), _stream(stream))
+    s, ctx = _on(stream)
+    with ctx:
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device=required_logits.device)
+        prm = params.as_struct()
+        st = lib.ls_sample_speculative(ptr, dt, rows, V, stride, int(num_decode), int(num_prefill),
+                                       int(num_speculative_tokens), _i32(gather_indices, "gather_indices"),
+                                       ctypes.byref(prm), int(step), int(bool(no_top_k)), int(bool(no_top_p)),
+                                       _i32(out, "out"),
+                                       _i32(out_token_to_request_index, "out_token_to_request_index"),
+                                       _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_sample_speculative")
     return out
@@ -200,14 +216,16 @@ def log_probs(logits, params, num_rows=None, gather_indices=None, token_to_reque
     ptr, dt, rows, V, stride = _logits_desc(logits)
     if num_rows is None:
         num_rows = len(gather_indices) if gather_indices is not None else rows
-    if out is None:
-        out = torch.empty((num_rows, V), dtype=torch.float32, device=logits.device)
-    if out.dtype != torch.float32 or not out.is_contiguous() or out.numel() < num_rows * V:
-        raise ValueError("out must be a contiguous float32 tensor of num_rows * vocab entries")
-    prm = params.as_struct()
-    st = lib.ls_log_probs(ptr, dt, rows, V, stride, int(num_rows), _i32(gather_indices, "gather_indices"),
-                          _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
-                          _dptr(out), _i32(error_word, "error_word"), _stream(stream))
+    s, ctx = _on(stream)
+    with ctx:
+        if out is None:
+            out = torch.empty((num_rows, V), dtype=torch.float32, device=logits.device)
+        if out.dtype != torch.float32 or not out.is_contiguous() or out.numel() < num_rows * V:
+            raise ValueError("out must be a contiguous float32 tensor of num_rows * vocab entries")
+        prm = params.as_struct()
+        st = lib.ls_log_probs(ptr, dt, rows, V, stride, int(num_rows), _i32(gather_indices, "gather_indices"),
+                              _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
+                              _dptr(out), _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_log_probs")
     return out
@@ -221,27 +239,29 @@ def sample_log_probs(logits, n, params, step, no_top_k, no_top_p, gather_indices
     import torch
     lib = load_library()
     ptr, dt, rows, V, stride = _logits_desc(logits)
-    if out is None:
-        out = torch.empty(n, dtype=torch.int32, device=logits.device)
-    if want_log_probs and out_log_probs is None:
-        out_log_probs = torch.empty((n, V), dtype=torch.float32, device=logits.device)
-    if want_selected and out_selected is None:
-        out_selected = torch.empty(n, dtype=torch.float32, device=logits.device)
-    if not want_log_probs:
-        out_log_probs = None
-    if not want_selected:
-        out_selected = None
-    if out_log_probs is not None and (out_log_probs.dtype != torch.float32 or not out_log_probs.is_contiguous()
-                                      or out_log_probs.numel() < n * V):
-        raise ValueError("out_log_probs must be a contiguous float32 tensor of n * vocab entries")
-    if out_selected is not None and (out_selected.dtype != torch.float32 or out_selected.numel() < n):
-        raise ValueError("out_selected must be a float32 tensor of n entries")
-    prm = params.as_struct()
-    st = lib.ls_sample_log_probs(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
-                                 _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
-                                 int(step), int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"),
-                                 _dptr(out_log_probs), _dptr(out_selected), _i32(error_word, "error_word"),
-                                 _stream(stream))
+    s, ctx = _on(stream)
+    with ctx:
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device=logits.device)
+        if want_log_probs and out_log_probs is None:
+            out_log_probs = torch.empty((n, V), dtype=torch.float32, device=logits.device)
+        if want_selected and out_selected is None:
+            out_selected = torch.empty(n, dtype=torch.float32, device=logits.device)
+        if not want_log_probs:
+            out_log_probs = None
+        if not want_selected:
+            out_selected = None
+        if out_log_probs is not None and (out_log_probs.dtype != torch.float32
+                                          or not out_log_probs.is_contiguous() or out_log_probs.numel() < n * V):
+            raise ValueError("out_log_probs must be a contiguous float32 tensor of n * vocab entries")
+        if out_selected is not None and (out_selected.dtype != torch.float32 or out_selected.numel() < n):
+            raise ValueError("out_selected must be a float32 tensor of n entries")
+        prm = params.as_struct()
+        st = lib.ls_sample_log_probs(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
+                                     _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
+                                     int(step), int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"),
+                                     _dptr(out_log_probs), _dptr(out_selected), _i32(error_word, "error_word"),
+                                     _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_sample_log_probs")
     return out, out_log_probs, out_selected
@@ -257,13 +277,15 @@ def sample_device_step(logits, n, params, step, no_top_k, no_top_p, gather_indic
     ptr, dt, rows, V, stride = _logits_desc(logits)
     if step.dtype not in (torch.int64, torch.uint64) or step.numel() != 1:
         raise TypeError("step must be a one-element int64/uint64 device tensor")
-    if out is None:
-        out = torch.empty(n, dtype=torch.int32, device=logits.device)
-    prm = params.as_struct()
-    st = lib.ls_sample_device_step(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
-                                   _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
-                                   _dptr(step), int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"),
-                                   _i32(error_word, "error_word"), _stream(stream))
+    s, ctx = _on(stream)
+    with ctx:
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device=logits.device)
+        prm = params.as_struct()
+        st = lib.ls_sample_device_step(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
+                                       _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
+                                       _dptr(step), int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"),
+                                       _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_sample_device_step")
     return out
@@ -277,10 +299,12 @@ def argmax(logits, n=None, gather_indices=None, out=None, error_word=None, strea
     ptr, dt, rows, V, stride = _logits_desc(logits)
     if n is None:
         n = len(gather_indices) if gather_indices is not None else rows
-    if out is None:
-        out = torch.empty(n, dtype=torch.int32, device=logits.device)
-    st = lib.ls_argmax(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"), _i32(out, "out"),
-                       _i32(error_word, "error_word"), _stream(stream))
+    s, ctx = _on(stream)
+    with ctx:
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device=logits.device)
+        st = lib.ls_argmax(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
+                           _i32(out, "out"), _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_argmax")
     return out
@@ -294,15 +318,18 @@ def verify_chain(candidates, target_sampled, predicts=None, accept_index=None, a
     lib = load_library()
     bs, n = candidates.shape
     dev = candidates.device
-    if predicts is None:
-        predicts = torch.full((bs * n,), -1, dtype=torch.int32, device=dev)
-    if accept_index is None:
-        accept_index = torch.empty((bs, n), dtype=torch.int32, device=dev)
-    if accept_token_num is None:
-        accept_token_num = torch.empty(bs, dtype=torch.int32, device=dev)
-    st = lib.ls_verify_chain(_i32(candidates.contiguous(), "candidates"), _i32(target_sampled, "target_sampled"),
-                             int(bs), int(n), _i32(predicts, "predicts"), _i32(accept_index, "accept_index"),
-                             _i32(accept_token_num, "accept_token_num"), _stream(stream))
+    s, ctx = _on(stream)
+    with ctx:
+        if predicts is None:
+            predicts = torch.full((bs * n,), -1, dtype=torch.int32, device=dev)
+        if accept_index is None:
+            accept_index = torch.empty((bs, n), dtype=torch.int32, device=dev)
+        if accept_token_num is None:
+            accept_token_num = torch.empty(bs, dtype=torch.int32, device=dev)
+        cand = candidates.contiguous()
+        st = lib.ls_verify_chain(_i32(cand, "candidates"), _i32(target_sampled, "target_sampled"),
+                                 int(bs), int(n), _i32(predicts, "predicts"), _i32(accept_index, "accept_index"),
+                                 _i32(accept_token_num, "accept_token_num"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_verify_chain")
     return predicts, accept_index, accept_token_num
@@ -317,17 +344,20 @@ def sample_verify(logits, candidates, params, step, no_top_k, no_top_p, gather_i
     ptr, dt, rows, V, stride = _logits_desc(logits)
     bs, n = candidates.shape
     dev = logits.device
-    target = torch.empty(bs * n, dtype=torch.int32, device=dev)
-    predicts = torch.full((bs * n,), -1, dtype=torch.int32, device=dev)
-    accept_index = torch.empty((bs, n), dtype=torch.int32, device=dev)
-    accept_token_num = torch.empty(bs, dtype=torch.int32, device=dev)
-    prm = params.as_struct()
-    st = lib.ls_sample_verify(ptr, dt, rows, V, stride, int(bs), int(n), _i32(gather_indices, "gather_indices"),
-                              ctypes.byref(prm), int(step), int(bool(no_top_k)), int(bool(no_top_p)),
-                              _i32(candidates.contiguous(), "candidates"), _i32(target, "target"),
-                              _i32(predicts, "predicts"), _i32(accept_index, "accept_index"),
-                              _i32(accept_token_num, "accept_token_num"), _i32(error_word, "error_word"),
-                              _stream(stream))
+    s, ctx = _on(stream)
+    with ctx:
+        target = torch.empty(bs * n, dtype=torch.int32, device=dev)
+        predicts = torch.full((bs * n,), -1, dtype=torch.int32, device=dev)
+        accept_index = torch.empty((bs, n), dtype=torch.int32, device=dev)
+        accept_token_num = torch.empty(bs, dtype=torch.int32, device=dev)
+        cand = candidates.contiguous()
+        prm = params.as_struct()
+        st = lib.ls_sample_verify(ptr, dt, rows, V, stride, int(bs), int(n),
+                                  _i32(gather_indices, "gather_indices"), ctypes.byref(prm), int(step),
+                                  int(bool(no_top_k)), int(bool(no_top_p)), _i32(cand, "candidates"),
+                                  _i32(target, "target"), _i32(predicts, "predicts"),
+                                  _i32(accept_index, "accept_index"), _i32(accept_token_num, "accept_token_num"),
+                                  _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_sample_verify")
     return target, predicts, accept_index, accept_token_num

@@ -67,7 +67,7 @@ def _check(out, where):
     check_ids(ids, ref, where)
     assert err == ref["error_word"], (where, err, ref["error_word"])
     assert err2 == rlp["error_word"], (where, err2, rlp["error_word"])
-    check_log_probs(lp, rlp["lp"], rlp["kept"], rlp["flags"], where)
+    check_log_probs(lp, rlp, where)
 
 
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
@@ -228,3 +228,29 @@ def test_largest_vocab(dtype):
     with pytest.raises(ls.LSError) as e:
         ls.sample(big, 1, prm, 0, False, False)
     assert e.value.status == 2  # LS_ERR_UNSUPPORTED
+
+
+def test_explicit_side_stream():
+    """Calls given a stream other than the current one allocate and fill their
+    outputs on that stream: the results equal those of the same calls on the
+    current stream, with nothing synchronised in between but that stream."""
+    import torch
+    import logits_sampling_gb300 as ls
+    w = W.make_decode(rows=24, vocab=9000)
+    x = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).cuda()
+    prm = ls.SamplingParams.from_host(w.temperature, w.top_k, w.top_p, w.seed)
+    ids0 = ls.sample(x, w.n, prm, 5, w.no_top_k, w.no_top_p)
+    f0 = ls.sample_log_probs(x, w.n, prm, 5, w.no_top_k, w.no_top_p)
+    cand = torch.from_numpy(np.random.default_rng(1).integers(0, 9000, (6, 4)).astype(np.int32)).cuda()
+    v0 = ls.verify_chain(cand, ids0[:24])
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(torch.cuda.Stream()):  # a third stream is current meanwhile
+        ids1 = ls.sample(x, w.n, prm, 5, w.no_top_k, w.no_top_p, stream=side)
+        f1 = ls.sample_log_probs(x, w.n, prm, 5, w.no_top_k, w.no_top_p, stream=side)
+        v1 = ls.verify_chain(cand, ids1[:24], stream=side)
+    side.synchronize()
+    assert torch.equal(ids0, ids1)
+    assert torch.equal(f0[0], f1[0]) and torch.equal(f0[1], f1[1]) and torch.equal(f0[2], f1[2])
+    assert all(torch.equal(a, b) for a, b in zip(v0, v1))
