@@ -228,6 +228,7 @@ def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     ls.load_library()
+    ls.set_split_policy(args.split)
     w = make_workload(args.workload, rank)
     x = to_device(w, device)
     copies = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, x.numel() * x.element_size()))) + 1)
@@ -380,6 +381,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[args.workload], "rows": w.n, "vocab": w.vocab, "call": args.call,
+                   "split": args.split,
                    "l2": f"{copies} rotating input copies ({copies * x.numel() * x.element_size() / 1e6:.0f} MB) "
                          f"> 2x L2", "parallelism": f"replicas x{world} (rows independent, no collective)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -419,6 +421,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--max-copies", type=int, default=8)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--split", type=int, default=0, choices=[0, -1, 1, 2, 4, 8],
+                    help="sampling kernel: 0 = chosen from the batch shape (default); 1, 2, 4, 8 = the streaming "
+                         "sampler with that many CTAs per row; -1 = the one-CTA row kernel")
     ap.add_argument("--call", choices=["sample", "fused", "separate", "argmax", "verify"], default="sample",
                     help="sample: ids (ls_sample); fused: ids, log-prob rows and selected log-probs from one "
                          "ls_sample_log_probs call; separate: ls_sample then ls_log_probs; argmax: the "

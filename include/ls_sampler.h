@@ -6,6 +6,8 @@
  * (temperature, exact top-k, exact top-p).  Every call is asynchronous on the
  * caller's CUDA stream, allocates nothing, never synchronises with the host
  * and launches one kernel (ls_sample_device_step and ls_sample_verify: two).
+ * The sampling calls split a row over a thread-block cluster of 2, 4 or 8
+ * CTAs when the batch is small (ls_set_split_policy).
  *
  * Conventions shared by all entry points
  * --------------------------------------
@@ -264,6 +266,27 @@ ls_status ls_sample_verify(const void* logits, ls_dtype dtype, int64_t logits_ro
                            uint64_t step, int no_top_k, int no_top_p, const int32_t* candidates,
                            int32_t* out_target_sampled, int32_t* predicts, int32_t* accept_index,
                            int32_t* accept_token_num, int32_t* error_word, void* stream);
+
+/*
+ * ls_set_split_policy -- which kernel the sampling calls that return ids only
+ * (ls_sample, ls_sample_speculative, ls_sample_device_step, ls_sample_verify,
+ * and ls_sample_log_probs with both optional outputs NULL) launch, for every
+ * later call in the process.  For tests and tuning: every choice computes the
+ * same sampler (ids may differ only where the parity exemption allows, since
+ * the row's mass is summed in another order).
+ *   0           chosen per call from the batch shape on the host (default):
+ *               one CTA per row for batches of at least 1.5x the SM count,
+ *               else 2, 4 or 8 CTAs per row (a thread-block cluster) while
+ *               that leaves fewer than two CTAs per SM and slices of at least
+ *               2048 entries
+ *   1, 2, 4, 8  the streaming sampler (candidates collected during the read
+ *               of the row) with that many CTAs per row
+ *   -1          the one-CTA row kernel that re-reads candidate groups after
+ *               the read of the row
+ * Returns LS_OK, or LS_ERR_INVALID_ARG for any other value (unchanged).
+ * Not synchronised with calls in flight on other host threads.
+ */
+int ls_set_split_policy(int ctas_per_row);
 
 /* Human-readable name of a status code (static storage). */
 const char* ls_status_string(ls_status s);

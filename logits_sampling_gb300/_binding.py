@@ -60,6 +60,8 @@ def load_library():
     lib.ls_status_string.restype = ctypes.c_char_p
     lib.ls_max_vocab.argtypes = [ci]
     lib.ls_max_vocab.restype = i64
+    lib.ls_set_split_policy.argtypes = [ci]
+    lib.ls_set_split_policy.restype = ci
     _lib = lib
     return lib
 
@@ -73,6 +75,15 @@ def status_string(status):
 
 def max_vocab(dtype=LS_DTYPE_BF16):
     return int(load_library().ls_max_vocab(dtype))
+
+
+def set_split_policy(ctas_per_row):
+    """ls_set_split_policy: 0 = per-call choice from the batch shape; 1, 2, 4, 8
+    = the streaming sampler with that many CTAs per row; -1 = the one-CTA row
+    kernel.  Applies to every later sampling call of the process."""
+    st = load_library().ls_set_split_policy(int(ctas_per_row))
+    if st != LS_OK:
+        raise LSError(st, "ls_set_split_policy")
 
 
 @dataclass

@@ -65,14 +65,22 @@ struct KernelArgs {
   float* out_lp;   // log-prob rows (MODE_LOGPROBS; MODE_BOTH when not NULL)
   float* out_sel;  // raw log-prob of the sampled id per row (MODE_BOTH, when not NULL)
   int32_t* error_word;
-  int32_t cand_cap;  // capacity of the shared-memory candidate list
+  int32_t cand_cap;   // capacity of the shared-memory candidate list
+  int32_t gslot_cap;  // group-maximum slots of one CTA's slice (split sampler)
+  int32_t ent_cap;    // capacity of the candidate-entry list (split sampler)
+  int32_t pool_cap;   // captured-group slots shared by the warps once their own are full (split sampler)
 };
 
 constexpr int kWarpList = 128;  // candidate groups a warp lists before loading them
 constexpr int kTieList = 32;    // ties of the maximum recorded while collecting
 // Slack of the top-p candidate bound: the entries below it carry at most
-// e^-kTopPSlack of the mass that the cut leaves out.
-constexpr float kTopPSlack = 0.25f;
+// e^-kTopPSlack of the mass that the cut leaves out.  The bound decides only
+// which entries are examined first; a build may override it (a negative slack
+// puts the bound above the cut, so every top-p row takes the full re-select).
+#ifndef LS_TOPP_SLACK
+#define LS_TOPP_SLACK 0.25f
+#endif
+constexpr float kTopPSlack = LS_TOPP_SLACK;
 
 // Group-maximum slots of a row: worst-case row alignment, rounded up to whole
 // 16-byte vectors (the candidate list that follows stays 16-byte aligned).

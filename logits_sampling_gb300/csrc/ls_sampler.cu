@@ -8,6 +8,67 @@ namespace lsg {
 extern template ls_status dispatch<MODE_SAMPLE>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
 extern template ls_status dispatch<MODE_LOGPROBS>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
 extern template ls_status dispatch<MODE_BOTH>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
+template <int C>
+ls_status dispatch_split(KernelArgs a, ls_dtype dtype, int route, int32_t n, cudaStream_t stream);
+extern template ls_status dispatch_split<1>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
+extern template ls_status dispatch_split<2>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
+extern template ls_status dispatch_split<4>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
+extern template ls_status dispatch_split<8>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
+
+// Which sampling kernel runs (ls_set_split_policy): 0 = chosen per call from
+// the batch shape; 1, 2, 4, 8 = the streaming sampler with that many CTAs per
+// row; -1 = the one-CTA row kernel without in-stream collection.
+static std::atomic<int> g_split_policy{0};
+
+static int sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices && (v = cache[dev].load(std::memory_order_relaxed)) > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Kernel from the batch shape alone (host values, no device read).  A batch
+// of at least one and a half times the SM count keeps every SM streaming with
+// one CTA per row: the row kernel.  A smaller batch with rows long enough to
+// split runs the streaming sampler, doubling the CTAs per row while that
+// leaves fewer than two per SM and slices of at least 2048 entries; short rows
+// of a small batch take the row kernel.
+static int split_for(int32_t n, int64_t vocab) {
+  const int pol = g_split_policy.load(std::memory_order_relaxed);
+  if (pol == -1 || pol == 1 || pol == 2 || pol == 4 || pol == 8) return pol;
+  const int sms = sm_count();
+  if (sms <= 0 || (int64_t)n * 2 >= (int64_t)sms * 3) return -1;
+  int c = 1;
+  while (c < 8 && (int64_t)n * c < 2 * (int64_t)sms && vocab / (2 * c) >= 2048) c *= 2;
+  return c > 1 ? c : -1;
+}
+
+// The largest vocab every kernel accepts on the current device: the one-CTA
+// row kernel's (4 bytes of shared memory per 16 logits) is the smallest.
+static int64_t max_vocab_all() {
+  const int lim = max_dyn_smem();
+  if (lim <= 0) return 0;
+  const int64_t ng = ((int64_t)lim - (int64_t)smem_bytes(0, 256)) / (int64_t)sizeof(float) + 1;
+  return ng * kGroup - (2 * kGroup - 1);
+}
+
+// The sampling calls' kernel (ids only).  Every call accepts the same
+// vocabularies (ls_max_vocab), whichever kernel runs.
+ls_status dispatch_sample(const KernelArgs& a, ls_dtype dtype, int route, int32_t n, cudaStream_t stream) {
+  const int64_t vmax = max_vocab_all();
+  if (vmax <= 0) return LS_ERR_CUDA;
+  if (a.vocab > vmax) return LS_ERR_UNSUPPORTED;
+  switch (split_for(n, a.vocab)) {
+    case -1: return dispatch<MODE_SAMPLE>(a, dtype, route, n, stream);
+    case 2: return dispatch_split<2>(a, dtype, route, n, stream);
+    case 4: return dispatch_split<4>(a, dtype, route, n, stream);
+    case 8: return dispatch_split<8>(a, dtype, route, n, stream);
+    default: return dispatch_split<1>(a, dtype, route, n, stream);
+  }
+}
 
 // Advances a device-resident Philox step word after the sampler that read it
 // (stream order: every CTA of the sampler has read the word before this runs).
@@ -33,7 +94,7 @@ ls_status ls_sample(const void* logits, ls_dtype dtype, int64_t logits_rows, int
   a.map_mode = token_to_request_index ? MAP_T2R : MAP_IDENTITY;
   a.out_ids = out_ids;
   const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
-  return dispatch<MODE_SAMPLE>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
+  return dispatch_sample(a, dtype, route, n, static_cast<cudaStream_t>(stream));
 }
 
 ls_status ls_sample_speculative(const void* required_logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
@@ -61,7 +122,7 @@ ls_status ls_sample_speculative(const void* required_logits, ls_dtype dtype, int
   a.out_ids = out_ids;
   a.out_t2r = out_token_to_request_index;
   const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
-  return dispatch<MODE_SAMPLE>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
+  return dispatch_sample(a, dtype, route, n, static_cast<cudaStream_t>(stream));
 }
 
 ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
@@ -97,7 +158,7 @@ ls_status ls_sample_device_step(const void* logits, ls_dtype dtype, int64_t logi
   a.out_ids = out_ids;
   const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const ls_status rc = dispatch<MODE_SAMPLE>(a, dtype, route, n, st);
+  const ls_status rc = dispatch_sample(a, dtype, route, n, st);
   if (rc != LS_OK) return rc;
   advance_step_kernel<<<1, 1, 0, st>>>(step);
   return cudaGetLastError() == cudaSuccess ? LS_OK : LS_ERR_CUDA;
@@ -122,8 +183,16 @@ ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits
   a.out_sel = out_selected_log_probs;
   const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
   if (!out_log_probs && !out_selected_log_probs)  // ids only: the sampling kernels
-    return dispatch<MODE_SAMPLE>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
+    return dispatch_sample(a, dtype, route, n, static_cast<cudaStream_t>(stream));
   return dispatch<MODE_BOTH>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
+}
+
+int ls_set_split_policy(int ctas_per_row) {
+  if (ctas_per_row != 0 && ctas_per_row != -1 && ctas_per_row != 1 && ctas_per_row != 2 && ctas_per_row != 4 &&
+      ctas_per_row != 8)
+    return (int)LS_ERR_INVALID_ARG;
+  g_split_policy.store(ctas_per_row, std::memory_order_relaxed);
+  return (int)LS_OK;
 }
 
 const char* ls_status_string(ls_status s) {
@@ -137,11 +206,8 @@ const char* ls_status_string(ls_status s) {
 }
 
 int64_t ls_max_vocab(ls_dtype dtype) {
-  (void)dtype;  // the limit is the same for both dtypes: 4 bytes of shared memory per 16 logits
-  const int lim = max_dyn_smem();
-  if (lim <= 0) return 0;
-  const int64_t ng = ((int64_t)lim - (int64_t)smem_bytes(0, 256)) / (int64_t)sizeof(float) + 1;
-  return ng * kGroup - (2 * kGroup - 1);
+  (void)dtype;  // the limit is the same for both dtypes
+  return max_vocab_all();
 }
 
 }  // extern "C"

@@ -10,7 +10,8 @@
 
 namespace lsg {
 
-extern template ls_status dispatch<MODE_SAMPLE>(KernelArgs, ls_dtype, int, int32_t, cudaStream_t);
+// the sampling calls' kernel choice (ls_sampler.cu)
+ls_status dispatch_sample(const KernelArgs& a, ls_dtype dtype, int route, int32_t n, cudaStream_t stream);
 
 // One thread per request: walk the positions while the drafts match.
 __global__ void verify_chain_kernel(const int32_t* candidates, const int32_t* target_sampled, int32_t bs, int32_t n,
@@ -81,7 +82,7 @@ ls_status ls_sample_verify(const void* logits, ls_dtype dtype, int64_t logits_ro
   a.out_ids = out_target_sampled;
   const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const ls_status rc = dispatch<MODE_SAMPLE>(a, dtype, route, (int32_t)n64, st);
+  const ls_status rc = dispatch_sample(a, dtype, route, (int32_t)n64, st);
   if (rc != LS_OK) return rc;
   return launch_verify(candidates, out_target_sampled, bs, num_tokens, predicts, accept_index, accept_token_num, st);
 }

@@ -25,3 +25,18 @@ def cuda_available():
         return torch.cuda.is_available()
     except Exception:  # pragma: no cover
         return False
+
+
+# Every kernel choice of the sampling calls (ls_set_split_policy): per-call
+# choice from the shape, the one-CTA row kernel, and the streaming sampler
+# with 1, 2, 4 and 8 CTAs per row.
+SPLIT_POLICIES = [0, -1, 1, 2, 4, 8]
+
+
+@pytest.fixture(params=SPLIT_POLICIES, ids=lambda c: f"split{c}")
+def split_policy(request):
+    import logits_sampling_gb300 as ls
+    ls.load_library()
+    ls.set_split_policy(request.param)
+    yield request.param
+    ls.set_split_policy(0)

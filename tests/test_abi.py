@@ -40,6 +40,15 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_split_policy_values(lib):
+    """ls_set_split_policy accepts 0, -1, 1, 2, 4, 8 and rejects anything else
+    on the host (no GPU needed)."""
+    for bad in (3, 5, 16, -2, 7):
+        assert lib.ls_set_split_policy(bad) == 1, bad
+    for good in (-1, 1, 2, 4, 8, 0):
+        assert lib.ls_set_split_policy(good) == 0, good
+
+
 def test_no_torch_in_the_abi():
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()

@@ -9,7 +9,8 @@ from logits_sampling_gb300 import workloads as W
 
 from gpu_util import check_ids, check_log_probs
 
-pytestmark = pytest.mark.gpu
+# every test runs under each kernel choice of the sampling calls
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("split_policy")]
 
 
 @pytest.fixture(scope="module", autouse=True)

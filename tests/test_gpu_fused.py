@@ -1,5 +1,5 @@
 """GPU parity of the fused call (ls_sample_log_probs): the ids equal ls_sample's
-for the same arguments; the log-prob rows and the selected token's raw
+for the same arguments (outside the exemption rows); the log-prob rows and the selected token's raw
 log-prob match the oracle; error rows; optional outputs."""
 import numpy as np
 import pytest
@@ -43,11 +43,15 @@ def _run(w, route=None, step=None, want_lp=True, want_sel=True, gather=None, t2r
 def _check(w, out, route=None, step=None, gather=None, t2r=None, where=""):
     ids, lp, sel, ids_s, err = out
     nk, np_ = (w.no_top_k, w.no_top_p) if route is None else route
-    assert np.array_equal(ids, ids_s), (where, np.nonzero(ids != ids_s)[0][:10])
     n = len(ids)
     ref = oracle.sample(w.logits, odt(w), n, w.temperature, w.top_k, w.top_p, w.seed,
                         step=w.step if step is None else step, no_top_k=nk, no_top_p=np_, gather_indices=gather,
                         token_to_request_index=t2r, want_lp=lp is not None)
+    # the same ids as ls_sample (which may run another kernel, summing the
+    # row's mass in another order) on every row outside the exemption
+    clear = ref["flags"] == 0
+    assert np.array_equal(ids[clear], ids_s[clear]), (where, np.nonzero((ids != ids_s) & clear)[0][:10])
+    check_ids(ids_s, ref, where + " ls_sample")
     assert err == ref["error_word"], (where, err, ref["error_word"])
     check_ids(ids, ref, where)
     if lp is not None:
