@@ -37,7 +37,13 @@ def load_library():
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with `python -m logits_sampling_gb300.build` "
                            "(there is no CPU fallback)")
-    lib = ctypes.CDLL(path)
+    _lib = configure(ctypes.CDLL(path))
+    return _lib
+
+
+def configure(lib):
+    """Declare the C signatures of include/ls_sampler.h on a loaded library
+    (the package's own, or a test-only variant build of the same sources)."""
     P, i32, i64, u64, ci = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
     PP = ctypes.POINTER(_Params)
     lib.ls_sample.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P]
@@ -62,7 +68,6 @@ def load_library():
     lib.ls_max_vocab.restype = i64
     lib.ls_set_split_policy.argtypes = [ci]
     lib.ls_set_split_policy.restype = ci
-    _lib = lib
     return lib
 
 

@@ -157,6 +157,25 @@ __device__ __forceinline__ void ld256(const void* p, uint32_t (&r)[8]) {
                : "l"(p));
 }
 
+// The same load under an L2 eviction policy (createpolicy): the log-prob
+// modes keep the row in L2 for the write pass (evict_last) and let that pass's
+// re-read go first (evict_first).
+__device__ __forceinline__ void ld256_hint(const void* p, uint32_t (&r)[8], uint64_t policy) {
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p), "l"(policy));
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
 template <>
@@ -238,6 +257,9 @@ struct RowView<bf16_tag> {
   __device__ __forceinline__ float at(int64_t j) const { return bf16_bits_to_float(row[j]); }
   __device__ __forceinline__ bool full(int g) const { return g >= g_full_lo && g <= g_full_hi; }
   __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords]) const { ld256(base + (size_t)g * 32, w); }
+  __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords], uint64_t pol) const {
+    ld256_hint(base + (size_t)g * 32, w, pol);
+  }
   __device__ __forceinline__ static void unpack(const uint32_t (&w)[kWords], float (&v)[kGroup]) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -333,6 +355,10 @@ struct RowView<float> {
   __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords]) const {
     ld256(base + (size_t)g * 64, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
     ld256(base + (size_t)g * 64 + 32, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
+  }
+  __device__ __forceinline__ void load_words(int g, uint32_t (&w)[kWords], uint64_t pol) const {
+    ld256_hint(base + (size_t)g * 64, *reinterpret_cast<uint32_t(*)[8]>(&w[0]), pol);
+    ld256_hint(base + (size_t)g * 64 + 32, *reinterpret_cast<uint32_t(*)[8]>(&w[8]), pol);
   }
   __device__ __forceinline__ static void unpack(const uint32_t (&w)[kWords], float (&v)[kGroup]) {
 #pragma unroll
@@ -728,33 +754,59 @@ __device__ __forceinline__ void row_error(const KernelArgs& a, int64_t i, int mo
   }
 }
 
-// Write out[j] = kept(v_j) ? value(v_j) : -inf over the whole row, with
-// 16-byte stores to the output where its alignment allows.
+// 16-byte store that is evicted first (the log-prob rows are written once and
+// not read back here).
+__device__ __forceinline__ void st_stream4(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// Write out[j] = kept(v_j) ? value(v_j) : -inf over the whole row.  The row
+// is read again (normally from L2) group by group with the streaming pass's
+// 256-bit loads, one group per thread at a time (more groups in flight were
+// measured slower), and each group's 16 outputs go out four at a time as
+// 16-byte streaming stores when their start is 16-byte aligned (the same for
+// every group of a row), else one by one.
 template <typename TIn, typename KeptF, typename ValF>
 __device__ __forceinline__ void write_row(const RowView<TIn>& rv, float* out, KeptF kept, ValF val) {
-  const int64_t V = rv.V;
+  using RVT = RowView<TIn>;
   const uintptr_t oa = reinterpret_cast<uintptr_t>(out);
-  int64_t head = (int64_t)(((16u - (oa & 15u)) & 15u) / 4u);
-  if ((oa & 3u) != 0u) head = V;  // not even float aligned: all scalar
-  if (head > V) head = V;
-  for (int64_t j = threadIdx.x; j < head; j += kThreads) {
-    const float v = rv.at(j);
-    out[j] = kept(v) ? val(v) : kNegInf;
-  }
-  const int64_t nq = (V - head) / 4;
-  for (int64_t q = threadIdx.x; q < nq; q += kThreads) {
-    const int64_t j = head + 4 * q;
-    float4 o;
-    float v0 = rv.at(j), v1 = rv.at(j + 1), v2 = rv.at(j + 2), v3 = rv.at(j + 3);
-    o.x = kept(v0) ? val(v0) : kNegInf;
-    o.y = kept(v1) ? val(v1) : kNegInf;
-    o.z = kept(v2) ? val(v2) : kNegInf;
-    o.w = kept(v3) ? val(v3) : kNegInf;
-    *reinterpret_cast<float4*>(out + j) = o;
-  }
-  for (int64_t j = head + 4 * nq + threadIdx.x; j < V; j += kThreads) {
-    const float v = rv.at(j);
-    out[j] = kept(v) ? val(v) : kNegInf;
+  const bool vec = (oa & 3u) == 0u && (((oa >> 2) - (uintptr_t)rv.off) & 3u) == 0u;
+  constexpr int U = 1;
+  const uint64_t pol = l2_evict_first_policy();  // the row's last use
+  for (int g0 = threadIdx.x; g0 < rv.NG; g0 += U * kThreads) {
+    uint32_t w[U][RVT::kWords];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + u * kThreads;
+      if (g < rv.NG && rv.full(g)) rv.load_words(g, w[u], pol);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + u * kThreads;
+      if (g < rv.NG) {
+        const bool full = rv.full(g);
+        if (!full) rv.load_words_partial(g, w[u]);
+        const int64_t j0 = rv.index(g, 0);
+#pragma unroll
+        for (int h = 0; h < kGroup / 4; ++h) {
+          float o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v = RVT::element_at(w[u], 4 * h + e);
+            o[e] = kept(v) ? val(v) : kNegInf;
+          }
+          if (vec && full) {
+            st_stream4(out + j0 + 4 * h, o[0], o[1], o[2], o[3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int64_t j = j0 + 4 * h + e;
+              if (j >= 0 && j < rv.V) out[j] = o[e];
+            }
+          }
+        }
+      }
+    }
   }
 }
 
@@ -806,10 +858,18 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   using RV = RowView<TIn>;
   constexpr int U = RV::kBytes == 2 ? 2 : 1;  // groups per stage
   constexpr int STEP = U * kThreads;
+  // log-prob modes: the row stays in L2 for the write pass (the rows in
+  // flight fit there; the outputs are stored evict-first)
+  const uint64_t keep = MODE == MODE_SAMPLE ? 0ull : l2_evict_last_policy();
   auto issue = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (rv.full(g0 + u * kThreads)) rv.load_words(g0 + u * kThreads, w[u]);
+      if (rv.full(g0 + u * kThreads)) {
+        if (MODE == MODE_SAMPLE)
+          rv.load_words(g0 + u * kThreads, w[u]);
+        else
+          rv.load_words(g0 + u * kThreads, w[u], keep);
+      }
   };
   uint32_t wa[U][RV::kWords], wb[U][RV::kWords];
   issue(tid, wa);
@@ -1238,8 +1298,15 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     // The masses are 2^(v c - R) = exp((v - M) / T) * 2^(M c - R); remove the
     // exactly computable residual of R's rounding from the normaliser.
     lnS -= fmaf(M, c, -R) * 0.6931471805599453f;
+    // (v - M) / T: a multiplication by RN(1/T) while |(v - M) / T| < 256 (an
+    // error below 3 2^-24 256 + half an ulp of the result, inside the 1e-4
+    // the log-probs are held to), the correctly rounded division beyond
+    const float invT = __frcp_rn(T), lim = 256.f * T;
     write_row(rv, a.out_lp + i * V, [&](float v) { return v >= lo_val; },
-              [&](float v) { return __fdiv_rn(v - M, T) - lnS; });
+              [&](float v) {
+                const float d = v - M;
+                return (fabsf(d) < lim ? d * invT : __fdiv_rn(d, T)) - lnS;
+              });
   }
 }
 

@@ -91,12 +91,14 @@ def logprob_tolerance(ref_lp_kept):
 
     1e-4 absolute wherever float32 holds that resolution.  Beyond it the bar
     is the rounding of the kernel's own arithmetic, which forms
-    lp = fl(fl(fl(v - M) / T) - ln S): the subtraction v - M and the
-    correctly rounded division each add at most half an ulp of
-    b = (v - M) / T (one and a half ulps of b once the first error is carried
-    through the division), and the final subtraction half an ulp of lp.  The
-    oracle's b is lp - max(lp) over the kept set (the maximum's log-prob is
-    -ln S).  For |lp| below about 500 the bar is 1e-4."""
+    lp = fl(fl(fl(v - M) / T) - ln S) once |b| = |(v - M) / T| >= 256: the
+    subtraction v - M and the correctly rounded division each add at most
+    half an ulp of b (one and a half ulps of b once the first error is carried
+    through the division), and the final subtraction half an ulp of lp.  (Below
+    |b| = 256 the kernel multiplies by RN(1/T) instead, within
+    3 2^-24 256 + half an ulp < 1e-4.)  The oracle's b is lp - max(lp) over
+    the kept set (the maximum's log-prob is -ln S).  For |lp| below about 500
+    the bar is 1e-4."""
     lp = np.asarray(ref_lp_kept, np.float64)
     b = lp - np.max(lp)
     return np.maximum(LOGPROB_ATOL, 1.5 * _ulp32(b) + 0.5 * _ulp32(lp))
