@@ -71,15 +71,22 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def ncu_traffic(workload):
-    """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+def traffic_key(workload, call, route, split=0):
+    """Key of profiles/traffic.json: the call on the workload's own route and
+    kernel choice, or on a forced one."""
+    return f"{workload}:{call}" + ("" if route == "auto" else f":{route}") + ("" if split == 0 else f":split{split}")
+
+
+def ncu_traffic(key):
+    """DRAM bytes per launch of the call's dominant kernel from the committed
+    ncu record (profiles/traffic.json), if it was taken on the current kernel
+    sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path))
     except (OSError, ValueError):
         return None
-    ent = rec.get(workload)
+    ent = rec.get(key)
     if not ent or ent.get("source_hash") != source_hash():
         return None
     return ent.get("dram_bytes_per_launch")
@@ -151,9 +158,18 @@ def barrier(world):
         dist.barrier()
 
 
-def make_workload(name, rank):
+ROUTES = {"auto": None, "kp": (False, False), "k": (False, True), "p": (True, False), "none": (True, True)}
+
+
+def make_workload(name, rank, route="auto", rows=0):
+    """The named workload (with `rows` > 0, that many rows of it: smaller
+    cases for profiler captures); `route` other than auto sets the batch flags
+    (no_top_k, no_top_p) that pick the kernel's route."""
     from logits_sampling_gb300 import workloads as W
-    return W.MAKERS[name]()
+    w = W.MAKERS[name](rows=rows) if rows > 0 and name != "speculative" else W.MAKERS[name]()
+    if ROUTES[route] is not None:
+        w.no_top_k, w.no_top_p = ROUTES[route]
+    return w
 
 
 def to_device(w, device):
@@ -192,7 +208,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     from logits_sampling_gb300 import workloads as W
-    w = make_workload(args.workload, rank)
+    w = make_workload(args.workload, rank, args.route, args.rows)
     rows = min(w.n, args.ref_rows)
     # size each step so that the whole run stays within about two minutes
     t = time.perf_counter()
@@ -229,7 +245,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     ls.load_library()
     ls.set_split_policy(args.split)
-    w = make_workload(args.workload, rank)
+    w = make_workload(args.workload, rank, args.route, args.rows)
     x = to_device(w, device)
     copies = max(2, int(np.ceil(2.0 * L2_BYTES / max(1, x.numel() * x.element_size()))) + 1)
     copies = min(copies, args.max_copies)
@@ -375,13 +391,14 @@ def run_ours(args, world, rank, local):
         alg_bytes = W.algorithmic_bytes(w) + W.algorithmic_bytes(w, with_log_probs=True)
     achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    traffic = ncu_traffic(args.workload) if args.call == "sample" else None
+    traffic = ncu_traffic(traffic_key(args.workload, args.call, args.route, args.split))
     line = {
         "metric": METRIC, "value": rows_per_s, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[args.workload], "rows": w.n, "vocab": w.vocab, "call": args.call,
-                   "split": args.split,
+        "config": {"workload": DESCRIPTIONS[args.workload] + (f" [{w.n} rows]" if args.rows else ""), "rows": w.n,
+                   "vocab": w.vocab, "call": args.call,
+                   "split": args.split, "route": args.route,
                    "l2": f"{copies} rotating input copies ({copies * x.numel() * x.element_size() / 1e6:.0f} MB) "
                          f"> 2x L2", "parallelism": f"replicas x{world} (rows independent, no collective)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -421,6 +438,12 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--max-copies", type=int, default=8)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="rows of the workload (0: its own; speculative keeps its own) -- smaller cases for "
+                         "profiler captures, not bench lines")
+    ap.add_argument("--route", choices=sorted(ROUTES), default="auto",
+                    help="batch flags: auto = the workload's own; kp, k, p, none = top-k and top-p, top-k only, "
+                         "top-p only, no filter (the flags switch the other filters off for every row)")
     ap.add_argument("--split", type=int, default=0, choices=[0, -1, 1, 2, 4, 8],
                     help="sampling kernel: 0 = chosen from the batch shape (default); 1, 2, 4, 8 = the streaming "
                          "sampler with that many CTAs per row; -1 = the one-CTA row kernel")
