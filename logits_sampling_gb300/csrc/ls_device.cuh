@@ -87,6 +87,25 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
   return c;
 }
 
+// Four Philox4x32-10 blocks at once (counters c[0..3], one key): the same
+// rounds as philox4x32_10, four independent chains per round, the ten rounds
+// kept a loop (a short body: it serves code that runs about once per warp).
+__device__ __forceinline__ void philox4x32_10_x4(uint4 (&c)[4], uint2 k) {
+#pragma unroll 1
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k.x += 0x9E3779B9u;
+      k.y += 0xBB67AE85u;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t lo0 = 0xD2511F53u * c[q].x, hi0 = __umulhi(0xD2511F53u, c[q].x);
+      const uint32_t lo1 = 0xCD9E8D57u * c[q].z, hi1 = __umulhi(0xCD9E8D57u, c[q].z);
+      c[q] = make_uint4(hi1 ^ c[q].y ^ k.x, lo1, hi0 ^ c[q].w ^ k.y, lo0);
+    }
+  }
+}
+
 // Noise word of vocabulary entry j for (seed, step, row): lane j%4 of
 // Philox(counter = (j/4, row, lo32 step, hi32 step), key = (lo32 seed, hi32 seed)).
 __device__ __forceinline__ uint32_t noise_word(uint64_t seed, uint64_t step, uint32_t row, int64_t j) {

@@ -393,20 +393,33 @@ __device__ __forceinline__ float max16(const float (&v)[kGroup]) {
   return fmaxf(fmaxf(a, b), fmaxf(c, d));
 }
 
+// Calls f(value, vocabulary index) for each entry >= lo of group g, in
+// order: one mask over the group's words, then a single call site for f (an
+// unrolled loop would copy f, often a Gumbel scorer with its Philox rounds,
+// sixteen times into the caller's code).
+template <typename RV, typename F>
+__device__ __forceinline__ void each_in_group(const RV& rv, int g, float lo, F&& f) {
+  uint32_t w[RV::kWords];
+  if (rv.full(g))
+    rv.load_words(g, w);
+  else
+    rv.load_words_partial(g, w);
+  uint32_t mm = RV::ge_mask(w, lo);
+#pragma unroll 1
+  while (mm) {
+    const int e = __ffs(mm) - 1;
+    mm &= mm - 1u;
+    f(RV::element(w, e), rv.index(g, e));
+  }
+}
+
 // Visit every row entry whose value is >= lo (NaN never qualifies), looking
 // only at groups whose maximum is >= lo.  Candidate groups are re-read from
 // global memory (normally still in L2 after the streaming pass).
 template <typename TIn, typename F>
 __device__ __forceinline__ void visit_candidates(const RowView<TIn>& rv, const float* gmax, float lo, F&& f) {
-  for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
-    if (gmax[g] >= lo) {
-      float v[kGroup];
-      rv.load(g, v);
-#pragma unroll
-      for (int e = 0; e < kGroup; ++e)
-        if (v[e] >= lo) f(v[e], rv.index(g, e));
-    }
-  }
+  for (int g = threadIdx.x; g < rv.NG; g += kThreads)
+    if (gmax[g] >= lo) each_in_group(rv, g, lo, f);
 }
 
 // The row entries that later phases examine.  After the streaming pass one
@@ -492,14 +505,14 @@ __device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float l
   lb -= fabsf(lb) * 1e-5f + 1e-30f;
   const float lo2 = fmaxf(lo, lb);
   PhiloxCache pc;
-  auto test = [&](float v, int64_t j) {
+  auto test_word = [&](float v, int64_t j, uint32_t x) {
     const float z = __fdiv_rn(v, T);
     const float need = s_lb - z - 1e-3f;
     const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
-    const uint32_t x = pc.word(seed, step, row, j);
     const float u = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
     if (u >= thr) atomicMax(&sh.best, argmax_key(z + gumbel_of_word(x), j));
   };
+  auto test = [&](float v, int64_t j) { test_word(v, j, pc.word(seed, step, row, j)); };
   if (cs.listed) {
     // each thread walks a contiguous run of the list (entries of one group are
     // consecutive there), so neighbouring entries share Philox blocks
@@ -561,13 +574,7 @@ __device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float l
             const uint4 bq = e8 < 4 ? p0 : p1;
             const uint32_t x = (e & 3) == 0 ? bq.x : (e & 3) == 1 ? bq.y : (e & 3) == 2 ? bq.z : bq.w;
             const float v = RVT::element_at(w, e);
-            if (v >= lo2 && v < M && (((x >> 9) << 1) | 1u) >= thr_i) {
-              const float z = __fdiv_rn(v, T);
-              const float need = s_lb - z - 1e-3f;
-              const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
-              const float u = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
-              if (u >= thr) atomicMax(&sh.best, argmax_key(z + gumbel_of_word(x), j0 + e));
-            }
+            if (v >= lo2 && v < M && (((x >> 9) << 1) | 1u) >= thr_i) test_word(v, j0 + e, x);
           }
         }
       } else {
@@ -739,6 +746,88 @@ __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo
     __syncthreads();        // the cut fields and the histogram are rewritten by the next level
   }
   return SelResult{klo, above + mass_at, false};
+}
+
+// Exact cuts over a short candidate list (at most kSmallList entries, all of
+// them listed) by direct counting: for each entry x, the number and the
+// fixed-point mass of the listed entries strictly above it.  x survives the
+// top-k cut iff fewer than k entries lie above it, and a top-p cut with
+// target t iff the mass strictly above it is below t -- the kept sets of
+// radix_select (the largest key whose upward-closed weight reaches the
+// target), without its per-level histograms and scans.  With k_on and p_on
+// the top-p target is p times the weight of the top-k set, as in the joint
+// level of radix_select.  Four threads share an entry, a quarter of the list
+// each.  The histogram area is the scratch.  Returns the final cut; for a
+// top-p cut alone whose candidates weigh less than the target, the short
+// result radix_select gives (the whole range from klo kept).
+constexpr int kSmallList = 128;
+static_assert(kThreads == 4 * kSmallList, "four threads per listed entry");
+
+template <typename TIn>
+__device__ SelResult small_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo, bool k_on, bool p_on, int32_t k,
+                                  float joint_p, unsigned long long target, float R, float c) {
+  using K = KeyOps<TIn>;
+  unsigned long long* ms = reinterpret_cast<unsigned long long*>(sh.hist);  // [kSmallList] masses
+  unsigned int* pc = sh.hist + 2 * kSmallList;                              // [4][kSmallList] counts above
+  unsigned long long* pm = ms + 3 * kSmallList;                             // [4][kSmallList] masses above
+  unsigned long long* cell = pm + 4 * kSmallList;                           // sum, kept mass, lowest kept key
+  static_assert(7 * kSmallList + 3 <= kBins, "scratch inside the histogram");
+  const int n = cs.count, t = threadIdx.x, lane = t & 31;
+  auto add_u64 = [](unsigned long long a, unsigned long long b) { return a + b; };
+  auto sum_into = [&](unsigned long long w, unsigned long long* dst) {
+    w = warp_reduce(w, add_u64);
+    if (lane == 0 && w) atomicAdd(dst, w);
+  };
+  if (t < n) ms[t] = mass_fixed(ex2(fmaf(cs.lv[t], c, -R)));
+  if (t < 3) cell[t] = t == 2 ? 0xFFFFFFFFull : 0ull;
+  __syncthreads();
+  const int x = t & (kSmallList - 1), q = t / kSmallList;
+  const bool own = q == 0 && x < n;  // the thread that decides entry x
+  const float vx = x < n ? cs.lv[x] : 0.f;
+  if (x < n) {
+    unsigned int cnt = 0u;
+    unsigned long long m = 0ull;
+    const int y1 = min(n, (q + 1) * (kSmallList / 4));
+    for (int y = q * (kSmallList / 4); y < y1; ++y) {
+      const bool gt = cs.lv[y] > vx;
+      cnt += gt ? 1u : 0u;
+      m += gt ? ms[y] : 0ull;
+    }
+    pc[q * kSmallList + x] = cnt;
+    pm[q * kSmallList + x] = m;
+  }
+  // the candidates' total mass (top-p alone) or the top-k set's (joint)
+  __syncthreads();
+  unsigned int cgt = 0u;
+  unsigned long long mgt = 0ull;
+  const unsigned long long mx = own ? ms[x] : 0ull;
+  if (own) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      cgt += pc[r * kSmallList + x];
+      mgt += pm[r * kSmallList + x];
+    }
+  }
+  bool keep = own && (!k_on || cgt < (unsigned int)k);
+  if (!k_on || p_on) {
+    sum_into(keep ? mx : 0ull, &cell[0]);
+    __syncthreads();
+    const unsigned long long w = cell[0];
+    if (k_on) {
+      target = __float2ull_ru(joint_p * __ull2float_rn(w));
+      if (target < 1ull) target = 1ull;
+    } else if (w < target) {
+      __syncthreads();  // every thread has read the total before the histogram is reused
+      return SelResult{klo, w, true};
+    }
+    keep = keep && mgt < target;
+  }
+  sum_into(keep ? mx : 0ull, &cell[1]);
+  if (keep) atomicMin(reinterpret_cast<unsigned int*>(&cell[2]), K::key(vx));
+  __syncthreads();
+  const SelResult r{(uint32_t)cell[2], cell[1], false};
+  __syncthreads();
+  return r;
 }
 
 __device__ __forceinline__ void row_error(const KernelArgs& a, int64_t i, int mode, int err) {
@@ -938,10 +1027,12 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // Each warp reduces its maximum, rescales every lane's sum to the warp's
   // reference RN(max * c) and adds; after one barrier every warp combines the
   // 16 warp results the same way (fixed order, so S is deterministic and the
-  // same in every warp).  For a top-k row each warp also extracts the j-th
-  // largest of its 32 thread maxima, j = ceil(k / 16): all 16 warps then hold
-  // >= j thread maxima (hence >= k distinct entries) at or above the smallest
-  // of those, gamma.
+  // same in every warp).  For a top-k row each of the w warps that streamed
+  // groups (thread t streamed groups t, t + 512, ...; w = 16 unless the row
+  // is short) also extracts the j-th largest of its 32 thread maxima,
+  // j = ceil(k / w): those warps then hold >= j w >= k thread maxima (distinct
+  // entries) at or above the smallest of those, gamma.
+  const int wact = min(kWarps, (rv.NG + 31) / 32);
   {
     uint4* h4 = reinterpret_cast<uint4*>(sh.hist);
     for (int q = tid; q < 2 * kBins / 4; q += kThreads) h4[q] = make_uint4(0u, 0u, 0u, 0u);
@@ -964,8 +1055,8 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       sw2 = warp_reduce(sw2, OpAddF());
     }
     float gj = kNegInf;
-    if (k_on && k <= 32 * kWarps) {
-      const int jrank = (k + kWarps - 1) / kWarps;
+    if (k_on && (tid >> 5) < wact && k <= 32 * wact) {
+      const int jrank = (k + wact - 1) / wact;
       float cur = m;
       for (int t = 0; t < jrank; ++t) {
         gj = warp_max(cur);
@@ -996,7 +1087,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   if (tid < 32) {
     const float mq = lane < kWarps ? sh.red_m[lane] : kNegInf;
     const float Mw = warp_max(mq);
-    const float gw = warp_min(lane < kWarps ? sh.red_f[lane] : kPosInf);
+    const float gw = warp_min(lane < wact ? sh.red_f[lane] : kPosInf);
     float Sw = 0.f, S2w = 0.f, Lpw = kNegInf;
     if (Mw > kNegInf && Mw < kPosInf) {
       if (need_sum) {
@@ -1250,11 +1341,14 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // ---- exact top-k and top-p cuts ---------------------------------------
   uint32_t lo_key = K::key(-FLT_MAX);  // no filter: every finite entry
   unsigned long long kept_mass = 0ull;
+  // a short list takes both cuts by direct counting
+  const bool small = kind != 0 && cs.listed && count <= kSmallList;
   if (kind != 0) {
     // the first level's histogram was built while collecting
     const unsigned long long target =
         kind == 1 ? (unsigned long long)k : max(1ull, __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale));
-    SelResult r1 = radix_select<TIn>(sh, cs, klo1, key_max, target, -1.f, R, c, 0ull, kind == 2, true);
+    SelResult r1 = small ? small_select<TIn>(sh, cs, klo1, k_on, p_on, k, fmaxf(p, 0.f), target, R, c)
+                         : radix_select<TIn>(sh, cs, klo1, key_max, target, -1.f, R, c, 0ull, kind == 2, true);
     if (kind == 2 && r1.short_total && lc > -FLT_MAX) {
       // The candidates weigh less than the top-p target, so the cut lies
       // below the bound: select again over every finite entry, visiting the
@@ -1266,7 +1360,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     lo_key = r1.key;
     kept_mass = r1.mass_ge;
   }
-  if (k_on && p_on) {
+  if (k_on && p_on && !small) {
     const SelResult r2 =
         radix_select<TIn>(sh, cs, lo_key, key_max, 0ull, fmaxf(p, 0.f), R, c, 0ull, true, false);
     lo_key = r2.key;

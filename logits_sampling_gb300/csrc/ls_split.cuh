@@ -55,17 +55,17 @@ struct SplitCfg<1> {
 };
 template <>
 struct SplitCfg<2> {
-  static constexpr int kB = 256, kMinBlocks = 4, kBinBits = 10;
+  static constexpr int kB = 256, kMinBlocks = 2, kBinBits = 10;
   static constexpr size_t kBudget = 112 * 1024;
 };
 template <>
 struct SplitCfg<4> {
-  static constexpr int kB = 128, kMinBlocks = 8, kBinBits = 10;
+  static constexpr int kB = 128, kMinBlocks = 4, kBinBits = 10;
   static constexpr size_t kBudget = 112 * 1024;
 };
 template <>
 struct SplitCfg<8> {
-  static constexpr int kB = 128, kMinBlocks = 8, kBinBits = 10;
+  static constexpr int kB = 128, kMinBlocks = 4, kBinBits = 10;
   static constexpr size_t kBudget = 112 * 1024;
 };
 
@@ -99,6 +99,12 @@ struct alignas(16) SplitShared {
   int cut_bin;
   int ecount;  // candidate entries gathered in the leader's list
   int pool;    // captured groups placed in the shared pool
+  // top-p probe rounds: per-CTA best score key and its value, per-CTA masses
+  unsigned long long pkey[kMaxCluster];
+  unsigned long long pabove[kMaxCluster], ptotal[kMaxCluster];
+  float pval[kMaxCluster];
+  unsigned long long red2_u64[kSplitWarps];
+  float bval;  // value of this CTA's best-scoring entry
 };
 
 // ---------------------------------------------------------------------------
@@ -191,6 +197,122 @@ struct Scorer {
   }
 };
 
+// A Scorer that also keeps the value of its best entry.
+struct ValueScorer {
+  Scorer s;
+  float bv;
+  __device__ __forceinline__ void operator()(float v, int64_t j) {
+    const unsigned long long before = s.best;
+    s(v, j);
+    if (s.best != before) bv = v;
+  }
+};
+
+// Smallest value of 2 (x >> 9) + 1, for the noise word x of an entry whose z
+// is at most fl(gm / T), that can still beat the best score key `best` (the
+// Scorer's test, 1e-3 looser in g): every entry of a group whose maximum is
+// gm needs u >= exp(-exp(z - s_best)) >= the group's level, and
+// u = (2 (x >> 9) + 1) 2^-24 >= thr implies 2 (x >> 9) + 1 >= floor(thr 2^24).
+// 0 (nothing rejected) while no best is held.
+__device__ __forceinline__ uint32_t group_word_threshold(unsigned long long best, float gm, float T) {
+  if (best == 0ull) return 0u;
+  const float need = f32_from_key((uint32_t)(best >> 32)) - __fdiv_rn(gm, T) - 1e-3f;
+  const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
+  return (uint32_t)(thr * 16777216.f);
+}
+
+// Per-warp buffer of the entries that passed a noise-word test (value,
+// vocabulary index).  Their exact tests run in batches with one entry per
+// lane: code that only a few entries reach then runs once per batch, instead
+// of once for every entry that some lane passes (a rarely taken branch into
+// code that other warps' code had evicted from the instruction caches).
+// `n` is the same in every lane; all lanes call push and flush.
+struct SurvivorBuffer {
+  float* v;
+  int32_t* j;
+  int cap;  // entries, a multiple of 32
+  int n;
+  template <typename S>
+  __device__ __forceinline__ void flush(S& sc) {
+    __syncwarp();
+    for (int q = (int)(threadIdx.x & 31); q < n; q += 32) sc(v[q], (int64_t)j[q]);
+    __syncwarp();
+    n = 0;
+  }
+  // Appends the entries of `surv` of a group (words w; idx(e): vocabulary
+  // index of entry e).
+  template <typename RV, typename Idx, typename S>
+  __device__ __forceinline__ void push(uint32_t surv, const uint32_t (&w)[RV::kWords], Idx idx, S& sc) {
+    const int lane = threadIdx.x & 31;
+    const int cnt = __popc(surv);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (tot == 0) return;
+    if (n + tot > cap) flush(sc);
+    if (tot > cap) {  // more than a whole buffer at once: exact tests in place
+      while (surv) {
+        const int e = __ffs(surv) - 1;
+        surv &= surv - 1u;
+        sc(RV::element(w, e), idx(e));
+      }
+      return;
+    }
+    int at = n + incl - cnt;
+    while (surv) {
+      const int e = __ffs(surv) - 1;
+      surv &= surv - 1u;
+      v[at] = RV::element(w, e);
+      j[at] = (int32_t)idx(e);
+      ++at;
+    }
+    n += tot;
+  }
+};
+
+// Entries of a group whose noise word clears the level thr_i (bit e for
+// entry e; only entries in `mm`).  A group whose first index j0 is a multiple
+// of 4 spans exactly four Philox blocks: they are drawn together, four
+// independent chains, and the sixteen tests need no branch; other groups
+// draw entry by entry.
+template <typename RV, typename Idx>
+__device__ __forceinline__ uint32_t word_survivors(uint32_t mm, int64_t j0, Idx idx, uint32_t thr_i, uint64_t seed,
+                                                   uint64_t step, uint32_t row, PhiloxCache& pc) {
+  if (mm == 0u || thr_i == 0u) return mm;
+  uint32_t surv = 0u;
+  if ((j0 & 3) == 0 && j0 >= 0) {
+    const uint32_t b0 = (uint32_t)((uint64_t)j0 >> 2);
+    uint4 c[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = make_uint4(b0 + q, row, (uint32_t)step, (uint32_t)(step >> 32));
+    philox4x32_10_x4(c, make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e) {
+      const uint4 bq = c[e >> 2];
+      const uint32_t x = (e & 3) == 0 ? bq.x : (e & 3) == 1 ? bq.y : (e & 3) == 2 ? bq.z : bq.w;
+      surv |= ((((x >> 9) << 1) | 1u) >= thr_i ? 1u : 0u) << e;
+    }
+    return surv & mm;
+  }
+  while (mm) {
+    const int e = __ffs(mm) - 1;
+    mm &= mm - 1u;
+    if ((((pc.word(seed, step, row, idx(e)) >> 9) << 1) | 1u) >= thr_i) surv |= 1u << e;
+  }
+  return surv;
+}
+
+// Smallest float above a finite x (the lower bound of "strictly above x").
+__device__ __forceinline__ float next_above(float x) {
+  if (x == 0.f) return __uint_as_float(1u);
+  const uint32_t b = __float_as_uint(x);
+  return __uint_as_float(x > 0.f ? b + 1u : b - 1u);
+}
+
 // Entry sources of the post-stream phases, per CTA:
 //   SRC_ENTRIES  the compacted list of candidate entries (value, index);
 //   SRC_GROUPS   the groups captured during the stream (their raw words and
@@ -261,23 +383,10 @@ struct SplitSource {
         }
       }
     } else if (mode == SRC_SLICE) {
-      for (int l = threadIdx.x; l < nl; l += B) {
-        if (gmax_value(gmax[l]) >= lo) {
-          float v[kGroup];
-          rv->load(gb + l, v);
-#pragma unroll
-          for (int e = 0; e < kGroup; ++e)
-            if (v[e] >= lo) f(v[e], rv->index(gb + l, e));
-        }
-      }
+      for (int l = threadIdx.x; l < nl; l += B)
+        if (gmax_value(gmax[l]) >= lo) each_in_group(*rv, gb + l, lo, f);
     } else {
-      for (int g = threadIdx.x; g < rv->NG; g += B) {
-        float v[kGroup];
-        rv->load(g, v);
-#pragma unroll
-        for (int e = 0; e < kGroup; ++e)
-          if (v[e] >= lo) f(v[e], rv->index(g, e));
-      }
+      for (int g = threadIdx.x; g < rv->NG; g += B) each_in_group(*rv, g, lo, f);
     }
   }
   // As each, but over the entry list a thread walks a contiguous run (the
@@ -483,13 +592,7 @@ struct WarpRow {
   const RowView<TIn>* rv;
   template <typename F>
   __device__ __forceinline__ void each(float lo, F&& f) const {
-    for (int g = threadIdx.x & 31; g < rv->NG; g += 32) {
-      float v[kGroup];
-      rv->load(g, v);
-#pragma unroll
-      for (int e = 0; e < kGroup; ++e)
-        if (v[e] >= lo) f(v[e], rv->index(g, e));
-    }
+    for (int g = threadIdx.x & 31; g < rv->NG; g += 32) each_in_group(*rv, g, lo, f);
   }
 };
 
@@ -592,6 +695,37 @@ __device__ __forceinline__ unsigned long long cta_max_key(SplitShared& sh, unsig
   return r;
 }
 
+// Block-wide sums of two 64-bit values (every thread gets both).
+template <int B>
+__device__ __forceinline__ void cta_sum2(SplitShared& sh, unsigned long long& x, unsigned long long& y) {
+  constexpr int W = B / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    y += __shfl_xor_sync(0xFFFFFFFFu, y, o);
+  }
+  if (lane == 0) {
+    sh.red_u64[warp] = x;
+    sh.red2_u64[warp] = y;
+  }
+  __syncthreads();
+  x = 0ull;
+  y = 0ull;
+#pragma unroll
+  for (int q = 0; q < W; ++q) {
+    x += sh.red_u64[q];
+    y += sh.red2_u64[q];
+  }
+  __syncthreads();
+}
+
+// Probe rounds a top-p row takes before it falls back to the select.
+constexpr int kProbeRounds = 4;
+// Captured groups over the row from which a top-p row probes instead of
+// gathering its candidates for the select.
+constexpr int kProbeGroups = 64;
+
 template <typename TIn, int ROUTE, int C>
 __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) split_sampler_kernel(const KernelArgs a) {
   using K = KeyOps<TIn>;
@@ -613,6 +747,10 @@ __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) spli
   float* es = reinterpret_cast<float*>(ej + a.ent_cap);  // Gumbel scores of the entries
   const int capw = (a.cand_cap - a.pool_cap) / W;  // own capture slots per warp
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the warp's survivor buffer in the entry list (rows without a filter, and
+  // top-p probes: neither gathers into that list while it is in use)
+  const int capb = (a.ent_cap / W) & ~31;
+  SurvivorBuffer sb{ev + warp * capb, ej + warp * capb, capb, 0};
   const uint32_t rank = C > 1 ? cluster_rank() : 0u;
   const int64_t i = (int64_t)(blockIdx.x / C);
   const bool lead = rank == 0u;
@@ -804,19 +942,51 @@ __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) spli
         }
         bound = fmaxf(bound, fmaxf(b, -FLT_MAX));  // -inf entries are never needed
       }
+      if constexpr (KD == KIND_FREE) {
+        if (first) {
+          // Warp seed: the exact score of the largest entry among the warp's
+          // groups of this stage, so that the thresholds prune from the first
+          // group on (without it every lane scores its first entries in full).
+          float gv = kNegInf;
+          int us = 0;
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (l0 + u * B < nl && gmv[u] > gv) {
+              gv = gmv[u];
+              us = u;
+            }
+          const float wv = warp_max(gv);
+          const unsigned holders = __ballot_sync(0xFFFFFFFFu, wv > kNegInf && gv == wv);
+          if (holders && lane == __ffs(holders) - 1) {
+            uint32_t ms = 0u;
+            int ls = l0;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (u == us) {
+                ms = RV::ge_mask(w[u], wv);
+                ls = l0 + u * B;
+              }
+            sc(wv, rv.index(gb + ls, __ffs(ms) - 1));
+          }
+          const unsigned long long kw = warp_max_key(sc.best);
+          if (kw > sc.best) sc.best = kw;
+        }
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int l = l0 + u * B;
         const bool over = l < nl && gmv[u] >= bound;
         if constexpr (KD == KIND_FREE) {
-          // Gumbel-max as a running maximum over the entries that can win
-          uint32_t mm = over ? RV::ge_mask(w[u], bound) : 0u;
-#pragma unroll 1
-          while (mm) {
-            const int e = __ffs(mm) - 1;
-            mm &= mm - 1u;
-            sc(RV::element(w[u], e), rv.index(gb + l, e));
-          }
+          // Gumbel-max as a running maximum over the entries that can win;
+          // a threshold taken at the group's largest z against the thread's
+          // best rejects most entries on their Philox word alone.
+          // (the survivors of the word test take their exact tests in
+          // batches: see SurvivorBuffer)
+          const uint32_t mm = over ? RV::ge_mask(w[u], bound) : 0u;
+          const uint32_t thr_i = mm ? group_word_threshold(sc.best, gmv[u], T) : 0u;
+          auto idx = [&](int e) { return rv.index(gb + l, e); };
+          const uint32_t surv = word_survivors<RV>(mm, rv.index(gb + l, 0), idx, thr_i, seed, sc.step, (uint32_t)i, sc.pc);
+          sb.push<RV>(surv, w[u], idx, sc);
         } else {
           // capture the groups whose maximum clears the bound into the warp's
           // own slots (k W + warp): a ballot places them, no atomics; once
@@ -856,6 +1026,7 @@ __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) spli
       stage(l0 + STEP, wb, false, it == 0);
       issue(l0 + 3 * STEP, wb);
     }
+    if constexpr (KD == KIND_FREE) sb.flush(sc);
     best = sc.best;
   };
   switch (kind) {
@@ -1057,6 +1228,130 @@ __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) spli
   const uint32_t key_max = K::key(M);
   const unsigned long long target =
       kind == KIND_TOPK ? (unsigned long long)k : max(1ull, __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale));
+
+  // ---- top-p alone over many candidates: probe the best scores ------------
+  // The Gumbel-max over the kept set is the best-scoring candidate whose
+  // value clears the cut, and an entry clears it iff the mass of the entries
+  // strictly above it is below the target (the kept set is the smallest
+  // upward-closed set whose mass reaches the target).  Each round scores the
+  // candidates >= lo in every CTA, takes the row's best over the cluster and
+  // tests it with one sum of masses: no histogram and no gathered list.  An
+  // entry that fails lies below the cut, so the next round raises lo above
+  // it (the candidates >= lo then still weigh at least the target).  After
+  // kProbeRounds rounds, or when the candidates weigh less than the target,
+  // the row falls through to the select.
+  {
+    int ncap = 0;
+#pragma unroll
+    for (int q = 0; q < C; ++q) ncap += max(sh.part[q].count, 0);
+    if (kind == KIND_TOPP && (overflow || ncap >= kProbeGroups)) {
+      srcs.mode = overflow ? SRC_SLICE : SRC_GROUPS;
+      // Scoring of this CTA's candidates >= lo (captured groups, or the slice
+      // re-read): a warp seed (the exact score of the largest entry among the
+      // lanes' first groups), then per group the threshold against the lane's
+      // best, so most entries are rejected on their Philox word alone.
+      auto score_pass = [&](float lo, ValueScorer& vs) {
+        const bool grp = srcs.mode == SRC_GROUPS;
+        const int nq = grp ? srcs.slots() : nl;
+        for (int q0 = 0; q0 < nq; q0 += B) {  // rounds: the same count in every thread
+          const int q = q0 + tid;
+          int l = -1;
+          uint32_t w[RV::kWords];
+          if (q < nq) {
+            if (grp) {
+              const int sl = srcs.slot(q);
+              if (sl >= 0 && gmax_value(gmax[cl[sl]]) >= lo) {
+                l = cl[sl];
+                srcs.load_group(sl, w);
+              }
+            } else if (gmax_value(gmax[q]) >= lo) {
+              l = q;
+              if (rv.full(gb + l))
+                rv.load_words(gb + l, w);
+              else
+                rv.load_words_partial(gb + l, w);
+            }
+          }
+          uint32_t mm = l >= 0 ? RV::ge_mask(w, lo) : 0u;
+          const float gm = mm ? RV::group_max(w) : kNegInf;
+          if (q0 == 0) {
+            const float wv = warp_max(gm);
+            const unsigned holders = __ballot_sync(0xFFFFFFFFu, wv > kNegInf && gm == wv);
+            if (holders) {
+              const int hl = __ffs(holders) - 1;
+              if (lane == hl) vs(wv, rv.index(gb + l, __ffs(RV::ge_mask(w, wv)) - 1));
+              vs.s.best = __shfl_sync(0xFFFFFFFFu, vs.s.best, hl);
+              vs.bv = __shfl_sync(0xFFFFFFFFu, vs.bv, hl);
+            }
+          }
+          // the entries whose word clears the group's level; their exact
+          // tests run in batches (SurvivorBuffer)
+          const uint32_t thr_i = mm ? group_word_threshold(vs.s.best, gm, T) : 0u;
+          auto idx = [&](int e) { return rv.index(gb + l, e); };
+          const uint32_t surv = word_survivors<RV>(mm, rv.index(gb + l, 0), idx, thr_i, seed, step, (uint32_t)i, vs.s.pc);
+          sb.push<RV>(surv, w, idx, vs);
+        }
+        sb.flush(vs);
+      };
+      float lo = lc;
+      for (int round = 0; round < kProbeRounds; ++round) {
+        ValueScorer vs{Scorer{T, seed, step, (uint32_t)i, false, 0ull, PhiloxCache{}}, 0.f};
+        score_pass(lo, vs);
+        const unsigned long long kc = cta_max_key<B>(sh, vs.s.best);
+        if (kc != 0ull && vs.s.best == kc) sh.bval = vs.bv;  // one thread: the index is in the key
+        __syncthreads();
+        if (tid < C) {
+          const uint32_t b = __float_as_uint(sh.bval);
+          if (C == 1) {
+            sh.pkey[0] = kc;
+            sh.pval[0] = sh.bval;
+          } else {
+            st_peer(peer(smem_u32(&sh.pkey[rank]), (uint32_t)tid), kc);
+            st_peer(peer(smem_u32(&sh.pval[rank]), (uint32_t)tid), b);
+          }
+        }
+        row_sync<C>();
+        unsigned long long kb = 0ull;
+        float vb = 0.f;
+#pragma unroll
+        for (int q = 0; q < C; ++q)
+          if (sh.pkey[q] > kb) {
+            kb = sh.pkey[q];
+            vb = sh.pval[q];
+          }
+        unsigned long long above = 0ull, total = 0ull;
+        srcs.each(lo, [&](float v, int64_t) {
+          const unsigned long long w = mass_fixed(ex2(fmaf(v, c, -R)));
+          total += w;
+          above += v > vb ? w : 0ull;
+        });
+        cta_sum2<B>(sh, above, total);
+        if (tid < C) {
+          if (C == 1) {
+            sh.pabove[0] = above;
+            sh.ptotal[0] = total;
+          } else {
+            st_peer(peer(smem_u32(&sh.pabove[rank]), (uint32_t)tid), above);
+            st_peer(peer(smem_u32(&sh.ptotal[rank]), (uint32_t)tid), total);
+          }
+        }
+        row_sync<C>();
+        unsigned long long A = 0ull, Tt = 0ull;
+#pragma unroll
+        for (int q = 0; q < C; ++q) {
+          A += sh.pabove[q];
+          Tt += sh.ptotal[q];
+        }
+        if (Tt < target || kb == 0ull) break;  // the cut lies below lc: the select re-selects
+        if (A < target) {
+          if (lead && tid == 0) a.out_ids[i] = argmax_index(kb);
+          return;  // no CTA reads another's shared memory after the last barrier
+        }
+        lo = next_above(vb);
+      }
+      srcs.mode = overflow ? SRC_SLICE : SRC_GROUPS;
+    }
+  }
 
   // ---- common case: gather the candidates at the leader -------------------
   // Every CTA's captured groups hold all of its slice's entries >= lc (unless
