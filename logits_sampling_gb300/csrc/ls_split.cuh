@@ -99,12 +99,18 @@ struct alignas(16) SplitShared {
   int cut_bin;
   int ecount;  // candidate entries gathered in the leader's list
   int pool;    // captured groups placed in the shared pool
-  // top-p probe rounds: per-CTA best score key and its value, per-CTA masses
-  unsigned long long pkey[kMaxCluster];
-  unsigned long long pabove[kMaxCluster], ptotal[kMaxCluster];
-  float pval[kMaxCluster];
-  unsigned long long red2_u64[kSplitWarps];
-  float bval;  // value of this CTA's best-scoring entry
+  // top-p probe rounds: per-CTA two best score keys and their values, the
+  // per-warp ones, per-CTA masses above each and in total
+  unsigned long long pkey[kMaxCluster][2];
+  float pval[kMaxCluster][2];
+  unsigned long long pabove[kMaxCluster][2], ptotal[kMaxCluster];
+  unsigned long long wkey[kSplitWarps][2];
+  float wval[kSplitWarps][2];
+  unsigned long long red2_u64[kSplitWarps], red3_u64[kSplitWarps];
+  // top-k bound refinement: this CTA's candidate counts per value bin, and
+  // every CTA's (all-gathered)
+  unsigned int lbin[32];
+  unsigned int kbin[kMaxCluster][32];
 };
 
 // ---------------------------------------------------------------------------
@@ -197,14 +203,61 @@ struct Scorer {
   }
 };
 
-// A Scorer that also keeps the value of its best entry.
-struct ValueScorer {
-  Scorer s;
-  float bv;
+// The two best score keys (k1 > k2, 0 when absent) and their entries'
+// values.
+struct TopTwo {
+  unsigned long long k1, k2;
+  float v1, v2;
+  __device__ __forceinline__ void add(unsigned long long k, float v) {
+    if (k > k1) {
+      k2 = k1;
+      v2 = v1;
+      k1 = k;
+      v1 = v;
+    } else if (k > k2 && k != k1) {
+      k2 = k;
+      v2 = v;
+    }
+  }
+  // Merge another pair (keys are unique per entry: an equal key is the same
+  // entry).
+  __device__ __forceinline__ void merge(const TopTwo& o) {
+    add(o.k2, o.v2);
+    add(o.k1, o.v1);
+  }
+  __device__ __forceinline__ void warp_merge() {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      TopTwo o;
+      o.k1 = __shfl_xor_sync(0xFFFFFFFFu, k1, off);
+      o.k2 = __shfl_xor_sync(0xFFFFFFFFu, k2, off);
+      o.v1 = __shfl_xor_sync(0xFFFFFFFFu, v1, off);
+      o.v2 = __shfl_xor_sync(0xFFFFFFFFu, v2, off);
+      merge(o);
+    }
+  }
+};
+
+// Gumbel-max scoring that keeps the two best entries: an entry takes its
+// exact score only if it can still beat the second best (the Scorer's test
+// against k2).
+struct TwoScorer {
+  float T;
+  uint64_t seed, step;
+  uint32_t row;
+  TopTwo t;
+  PhiloxCache pc;
   __device__ __forceinline__ void operator()(float v, int64_t j) {
-    const unsigned long long before = s.best;
-    s(v, j);
-    if (s.best != before) bv = v;
+    const float z = __fdiv_rn(v, T);
+    const uint32_t x = pc.word(seed, step, row, j);
+    if (t.k2 != 0ull) {
+      const float s_lb = f32_from_key((uint32_t)(t.k2 >> 32));
+      const float need = s_lb - z - 1e-3f;
+      const float thr = ex2(-ex2(-need * kLog2e) * kLog2e) * (1.f - 4e-7f);
+      const float u = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
+      if (!(u >= thr)) return;
+    }
+    t.add(argmax_key(z + gumbel_of_word(x), j), v);
   }
 };
 
@@ -720,8 +773,39 @@ __device__ __forceinline__ void cta_sum2(SplitShared& sh, unsigned long long& x,
   __syncthreads();
 }
 
+// Block-wide sums of three 64-bit values (every thread gets them).
+template <int B>
+__device__ __forceinline__ void cta_sum3(SplitShared& sh, unsigned long long& x, unsigned long long& y,
+                                         unsigned long long& z) {
+  constexpr int W = B / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    y += __shfl_xor_sync(0xFFFFFFFFu, y, o);
+    z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+  }
+  if (lane == 0) {
+    sh.red_u64[warp] = x;
+    sh.red2_u64[warp] = y;
+    sh.red3_u64[warp] = z;
+  }
+  __syncthreads();
+  x = y = z = 0ull;
+#pragma unroll
+  for (int q = 0; q < W; ++q) {
+    x += sh.red_u64[q];
+    y += sh.red2_u64[q];
+    z += sh.red3_u64[q];
+  }
+  __syncthreads();
+}
+
 // Probe rounds a top-p row takes before it falls back to the select.
 constexpr int kProbeRounds = 4;
+// Gathered lists up to this length take their cuts in the whole leader CTA by
+// direct counting (one entry per thread).
+constexpr int kLeadList = 128;
 // Captured groups over the row from which a top-p row probes instead of
 // gathering its candidates for the select.
 constexpr int kProbeGroups = 64;
@@ -1229,6 +1313,42 @@ __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) spli
   const unsigned long long target =
       kind == KIND_TOPK ? (unsigned long long)k : max(1ull, __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale));
 
+  // ---- top-k: a bound from the whole row -----------------------------------
+  // Each CTA's bound guarantees k entries in its own slice, so the row's bound
+  // (the largest of them) lies well below the row's k-th largest entry.  The
+  // candidates counted in 32 value bins over [lc, M], summed over the
+  // cluster, raise it to half a bin below the highest bin edge with at least
+  // k entries above (half a bin absorbs the rounding of the binning): the
+  // gathered list then holds little more than k entries.
+  if (kind == KIND_TOPK && !overflow && lc < M) {
+    constexpr int NT = 32;
+    const float scale = (float)NT / (M - lc);
+    if (tid < NT) sh.lbin[tid] = 0u;
+    __syncthreads();
+    srcs.mode = SRC_GROUPS;
+    srcs.each(lc, [&](float v, int64_t) { atomicAdd(&sh.lbin[min(NT - 1, (int)((v - lc) * scale))], 1u); });
+    __syncthreads();
+    for (int t = tid; t < NT * C; t += B) {
+      const int q = t / NT, b = t % NT;
+      if (C == 1)
+        sh.kbin[0][b] = sh.lbin[b];
+      else
+        st_peer(peer(smem_u32(&sh.kbin[rank][b]), (uint32_t)q), sh.lbin[b]);
+    }
+    row_sync<C>();
+    unsigned int cum = 0u;
+    int bk = 0;
+    for (int b = NT - 1; b > 0; --b) {
+#pragma unroll
+      for (int q = 0; q < C; ++q) cum += sh.kbin[q][b];
+      if (cum >= (unsigned int)k) {
+        bk = b;
+        break;
+      }
+    }
+    if (bk > 0) lc = fmaxf(lc, lc + ((float)bk - 0.5f) / scale);
+  }
+
   // ---- top-p alone over many candidates: probe the best scores ------------
   // The Gumbel-max over the kept set is the best-scoring candidate whose
   // value clears the cut, and an entry clears it iff the mass of the entries
@@ -1250,7 +1370,7 @@ __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) spli
       // re-read): a warp seed (the exact score of the largest entry among the
       // lanes' first groups), then per group the threshold against the lane's
       // best, so most entries are rejected on their Philox word alone.
-      auto score_pass = [&](float lo, ValueScorer& vs) {
+      auto score_pass = [&](float lo, TwoScorer& ts) {
         const bool grp = srcs.mode == SRC_GROUPS;
         const int nq = grp ? srcs.slots() : nl;
         for (int q0 = 0; q0 < nq; q0 += B) {  // rounds: the same count in every thread
@@ -1275,79 +1395,100 @@ __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) spli
           uint32_t mm = l >= 0 ? RV::ge_mask(w, lo) : 0u;
           const float gm = mm ? RV::group_max(w) : kNegInf;
           if (q0 == 0) {
-            const float wv = warp_max(gm);
-            const unsigned holders = __ballot_sync(0xFFFFFFFFu, wv > kNegInf && gm == wv);
-            if (holders) {
-              const int hl = __ffs(holders) - 1;
-              if (lane == hl) vs(wv, rv.index(gb + l, __ffs(RV::ge_mask(w, wv)) - 1));
-              vs.s.best = __shfl_sync(0xFFFFFFFFu, vs.s.best, hl);
-              vs.bv = __shfl_sync(0xFFFFFFFFu, vs.bv, hl);
-            }
+            // warp seed: exact scores of the largest entries of the two lanes
+            // with the largest group maxima, merged into every lane
+            const float wv1 = warp_max(gm);
+            const unsigned h1 = __ballot_sync(0xFFFFFFFFu, wv1 > kNegInf && gm == wv1);
+            const int l1 = h1 ? __ffs(h1) - 1 : -1;
+            const float gm2 = lane == l1 ? kNegInf : gm;
+            const float wv2 = warp_max(gm2);
+            const unsigned h2 = __ballot_sync(0xFFFFFFFFu, wv2 > kNegInf && gm2 == wv2);
+            const int l2 = h2 ? __ffs(h2) - 1 : -1;
+            if (lane == l1 || lane == l2) ts(gm, rv.index(gb + l, __ffs(RV::ge_mask(w, gm)) - 1));
+            ts.t.warp_merge();
           }
-          // the entries whose word clears the group's level; their exact
-          // tests run in batches (SurvivorBuffer)
-          const uint32_t thr_i = mm ? group_word_threshold(vs.s.best, gm, T) : 0u;
+          // the entries whose word clears the group's level against the
+          // second best; their exact tests run in batches (SurvivorBuffer)
+          const uint32_t thr_i = mm ? group_word_threshold(ts.t.k2, gm, T) : 0u;
           auto idx = [&](int e) { return rv.index(gb + l, e); };
-          const uint32_t surv = word_survivors<RV>(mm, rv.index(gb + l, 0), idx, thr_i, seed, step, (uint32_t)i, vs.s.pc);
-          sb.push<RV>(surv, w, idx, vs);
+          const uint32_t surv = word_survivors<RV>(mm, rv.index(gb + l, 0), idx, thr_i, seed, step, (uint32_t)i, ts.pc);
+          sb.push<RV>(surv, w, idx, ts);
         }
-        sb.flush(vs);
+        sb.flush(ts);
       };
       float lo = lc;
       for (int round = 0; round < kProbeRounds; ++round) {
-        ValueScorer vs{Scorer{T, seed, step, (uint32_t)i, false, 0ull, PhiloxCache{}}, 0.f};
-        score_pass(lo, vs);
-        const unsigned long long kc = cta_max_key<B>(sh, vs.s.best);
-        if (kc != 0ull && vs.s.best == kc) sh.bval = vs.bv;  // one thread: the index is in the key
+        TwoScorer ts{T, seed, step, (uint32_t)i, TopTwo{0ull, 0ull, 0.f, 0.f}, PhiloxCache{}};
+        score_pass(lo, ts);
+        // the CTA's two best, then the row's (all-gathered over the cluster)
+        ts.t.warp_merge();
+        if (lane == 0) {
+          sh.wkey[warp][0] = ts.t.k1;
+          sh.wkey[warp][1] = ts.t.k2;
+          sh.wval[warp][0] = ts.t.v1;
+          sh.wval[warp][1] = ts.t.v2;
+        }
         __syncthreads();
+        TopTwo ct{0ull, 0ull, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < W; ++q) ct.merge(TopTwo{sh.wkey[q][0], sh.wkey[q][1], sh.wval[q][0], sh.wval[q][1]});
         if (tid < C) {
-          const uint32_t b = __float_as_uint(sh.bval);
           if (C == 1) {
-            sh.pkey[0] = kc;
-            sh.pval[0] = sh.bval;
+            sh.pkey[0][0] = ct.k1;
+            sh.pkey[0][1] = ct.k2;
+            sh.pval[0][0] = ct.v1;
+            sh.pval[0][1] = ct.v2;
           } else {
-            st_peer(peer(smem_u32(&sh.pkey[rank]), (uint32_t)tid), kc);
-            st_peer(peer(smem_u32(&sh.pval[rank]), (uint32_t)tid), b);
+            const uint32_t q = (uint32_t)tid;
+            st_peer(peer(smem_u32(&sh.pkey[rank][0]), q), ct.k1);
+            st_peer(peer(smem_u32(&sh.pkey[rank][1]), q), ct.k2);
+            st_peer(peer(smem_u32(&sh.pval[rank][0]), q), __float_as_uint(ct.v1));
+            st_peer(peer(smem_u32(&sh.pval[rank][1]), q), __float_as_uint(ct.v2));
           }
         }
         row_sync<C>();
-        unsigned long long kb = 0ull;
-        float vb = 0.f;
+        TopTwo rt{0ull, 0ull, 0.f, 0.f};
 #pragma unroll
-        for (int q = 0; q < C; ++q)
-          if (sh.pkey[q] > kb) {
-            kb = sh.pkey[q];
-            vb = sh.pval[q];
-          }
-        unsigned long long above = 0ull, total = 0ull;
+        for (int q = 0; q < C; ++q) rt.merge(TopTwo{sh.pkey[q][0], sh.pkey[q][1], sh.pval[q][0], sh.pval[q][1]});
+        // masses strictly above each of the two, and of every candidate
+        unsigned long long above1 = 0ull, above2 = 0ull, total = 0ull;
         srcs.each(lo, [&](float v, int64_t) {
           const unsigned long long w = mass_fixed(ex2(fmaf(v, c, -R)));
           total += w;
-          above += v > vb ? w : 0ull;
+          above1 += v > rt.v1 ? w : 0ull;
+          above2 += v > rt.v2 ? w : 0ull;
         });
-        cta_sum2<B>(sh, above, total);
+        cta_sum3<B>(sh, above1, above2, total);
         if (tid < C) {
           if (C == 1) {
-            sh.pabove[0] = above;
+            sh.pabove[0][0] = above1;
+            sh.pabove[0][1] = above2;
             sh.ptotal[0] = total;
           } else {
-            st_peer(peer(smem_u32(&sh.pabove[rank]), (uint32_t)tid), above);
-            st_peer(peer(smem_u32(&sh.ptotal[rank]), (uint32_t)tid), total);
+            const uint32_t q = (uint32_t)tid;
+            st_peer(peer(smem_u32(&sh.pabove[rank][0]), q), above1);
+            st_peer(peer(smem_u32(&sh.pabove[rank][1]), q), above2);
+            st_peer(peer(smem_u32(&sh.ptotal[rank]), q), total);
           }
         }
         row_sync<C>();
-        unsigned long long A = 0ull, Tt = 0ull;
+        unsigned long long A1 = 0ull, A2 = 0ull, Tt = 0ull;
 #pragma unroll
         for (int q = 0; q < C; ++q) {
-          A += sh.pabove[q];
+          A1 += sh.pabove[q][0];
+          A2 += sh.pabove[q][1];
           Tt += sh.ptotal[q];
         }
-        if (Tt < target || kb == 0ull) break;  // the cut lies below lc: the select re-selects
-        if (A < target) {
-          if (lead && tid == 0) a.out_ids[i] = argmax_index(kb);
+        if (Tt < target || rt.k1 == 0ull) break;  // the cut lies below lc: the select re-selects
+        // the best is kept: it wins; else the second best, if kept, wins
+        // (every entry scoring above it is the best)
+        const unsigned long long win = A1 < target ? rt.k1 : rt.k2 != 0ull && A2 < target ? rt.k2 : 0ull;
+        if (win != 0ull) {
+          if (lead && tid == 0) a.out_ids[i] = argmax_index(win);
           return;  // no CTA reads another's shared memory after the last barrier
         }
-        lo = next_above(vb);
+        // both lie below the cut
+        lo = next_above(rt.k2 != 0ull ? fmaxf(rt.v1, rt.v2) : rt.v1);
       }
       srcs.mode = overflow ? SRC_SLICE : SRC_GROUPS;
     }
@@ -1419,6 +1560,48 @@ __global__ void __launch_bounds__(SplitCfg<C>::kB, SplitCfg<C>::kMinBlocks) spli
     if (C > 1) cluster_sync_all();
     if (E <= a.ent_cap) {
       if (!lead) return;  // nothing touches this CTA's shared memory any more
+      // A short list: the leader CTA takes the cuts by direct counting (one
+      // entry per thread: the count and the fixed-point mass of the entries
+      // strictly above it; kept by top-k iff fewer than k lie above, by a
+      // top-p target t iff the mass above is below t, the target of the joint
+      // route p times the top-k set's mass), then the best stored score among
+      // the kept entries.  A top-p cut whose candidates weigh less than the
+      // target goes on to the warp's re-select below.
+      if (E <= kLeadList) {
+        unsigned long long* ms = reinterpret_cast<unsigned long long*>(hist);
+        const bool own = tid < E;
+        const float vx = own ? ev[tid] : 0.f;
+        const unsigned long long mx = own ? mass_fixed(ex2(fmaf(vx, c, -R))) : 0ull;
+        if (own) ms[tid] = mx;
+        __syncthreads();
+        unsigned int cgt = 0u;
+        unsigned long long mgt = 0ull;
+        if (own)
+          for (int y = 0; y < E; ++y) {
+            const bool gt = ev[y] > vx;
+            cgt += gt ? 1u : 0u;
+            mgt += gt ? ms[y] : 0ull;
+          }
+        bool keep = own && (kind != KIND_TOPK || cgt < (unsigned int)k);
+        bool decided = true;
+        if (kind == KIND_TOPP || p_on) {
+          unsigned long long w = keep ? mx : 0ull, unused = 0ull;
+          cta_sum2<B>(sh, w, unused);
+          unsigned long long tg = target;
+          if (kind == KIND_TOPK) {
+            tg = __float2ull_ru(fmaxf(p, 0.f) * __ull2float_rn(w));
+            if (tg < 1ull) tg = 1ull;
+          } else if (w < target) {
+            decided = false;
+          }
+          keep = keep && mgt < tg;
+        }
+        if (decided) {
+          const unsigned long long kb = cta_max_key<B>(sh, keep ? argmax_key(es[tid], ej[tid]) : 0ull);
+          if (tid == 0) a.out_ids[i] = argmax_index(kb);
+          return;
+        }
+      }
       // The leader's warp 0 finishes the row alone: the cuts over the entry
       // list (warp-level selects), then the best stored score at or above the
       // cut.  The other warps are done.

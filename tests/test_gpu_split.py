@@ -79,3 +79,34 @@ def test_flat_rows_overflow_the_lists(policy):
         ids, err, _ = gpu_sample(w)
         assert err == 0
         check_ids(ids, oracle_sample(w), f"flat {dt} split {policy}")
+
+
+def _probe_case(dt):
+    key = ("probe", dt)
+    if key not in _REF:
+        rng = np.random.default_rng(47)
+        rows, V = 16, 32000
+        x = (rng.standard_normal((rows, V)) * 3.0).astype(np.float32)
+        logits = W.to_bf16_bits(x) if dt == W.BF16 else x
+        w = W.Workload("probe", dt, logits, rows, temperature=np.full(rows, 2.0, np.float32),
+                       top_k=np.zeros(rows, np.int32),
+                       top_p=np.array([0.001, 0.01, 0.05, 0.2, 0.5, 0.8, 0.9, 0.95] * 2, np.float32),
+                       seed=np.arange(rows, dtype=np.uint64) + 7, no_top_k=True, no_top_p=False)
+        _REF[key] = (w, oracle_sample(w))
+    return _REF[key]
+
+
+@pytest.mark.parametrize("dt", [W.BF16, W.F32])
+@pytest.mark.parametrize("policy", [1, 2, 4, 8], ids=lambda c: f"split{c}")
+def test_topp_probe_rounds(policy, dt):
+    """Flat rows under top-p alone keep thousands of candidates.  With a small
+    p the kept set is the top few entries while the best Gumbel scores lie
+    anywhere among the candidates: the streaming sampler's probe rounds reject
+    the best-scoring candidate round after round and, after the last round,
+    fall back to the select; larger p answers within the first rounds."""
+    import logits_sampling_gb300 as ls
+    ls.set_split_policy(policy)
+    w, ref = _probe_case(dt)
+    ids, err, _ = gpu_sample(w)
+    assert err == 0
+    check_ids(ids, ref, f"probe {dt} split {policy}")
