@@ -52,6 +52,7 @@
 #ifndef LS_SAMPLER_H
 #define LS_SAMPLER_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -145,11 +146,26 @@ ls_status ls_sample_speculative(const void* required_logits, ls_dtype dtype, int
  * reads logits row i).
  *
  *   out_log_probs   device float[num_rows * vocab], row-major, written fully
+ *   workspace       NULL, or device memory of at least
+ *                   ls_log_probs_workspace_bytes(num_rows) bytes, 16-byte
+ *                   aligned, owned by the caller and not used by other calls
+ *                   in flight (otherwise LS_ERR_INVALID_ARG).  With a
+ *                   workspace, a batch whose logits fit in 60% of L2 takes two
+ *                   launches: the row kernel leaves 16 bytes of scalars per row
+ *                   there, and a second kernel writes the rows in tiles spread
+ *                   over every SM (the same values).  Without one, or for a
+ *                   larger batch, the row kernel writes each row itself.
+ *   workspace_bytes size of workspace (ignored when it is NULL)
  * Other arguments as for ls_sample.
  */
 ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
                        int32_t num_rows, const int32_t* gather_indices, const int32_t* token_to_request_index,
-                       const ls_params* params, float* out_log_probs, int32_t* error_word, void* stream);
+                       const ls_params* params, float* out_log_probs, void* workspace, size_t workspace_bytes,
+                       int32_t* error_word, void* stream);
+
+/* Bytes of the optional workspace of ls_log_probs and ls_sample_log_probs for
+ * num_rows rows (16 per row; 0 when num_rows <= 0). */
+size_t ls_log_probs_workspace_bytes(int32_t num_rows);
 
 /*
  * ls_sample_device_step -- ls_sample with the Philox step word in device
@@ -195,6 +211,8 @@ ls_status ls_sample_device_step(const void* logits, ls_dtype dtype, int64_t logi
  *                          filter): l_id - ln sum_j exp(l_j) over the row, NaN
  *                          logits read as -inf; a row whose maximum is +inf
  *                          gives -ln(#(+inf entries)) for a +inf id
+ *   workspace, workspace_bytes
+ *                          as for ls_log_probs (used only with out_log_probs)
  * With both optional outputs NULL the call is ls_sample.  Error rows: id -1,
  * NaN log-probs.  Other arguments as for ls_sample.
  */
@@ -202,7 +220,8 @@ ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits
                               int64_t row_stride, int32_t n, const int32_t* gather_indices,
                               const int32_t* token_to_request_index, const ls_params* params, uint64_t step,
                               int no_top_k, int no_top_p, int32_t* out_ids, float* out_log_probs,
-                              float* out_selected_log_probs, int32_t* error_word, void* stream);
+                              float* out_selected_log_probs, void* workspace, size_t workspace_bytes,
+                              int32_t* error_word, void* stream);
 
 /*
  * ls_argmax -- the all-greedy fast path: out_ids[i] = the lowest index of the

@@ -50,9 +50,12 @@ def configure(lib):
     lib.ls_sample.restype = ci
     lib.ls_sample_speculative.argtypes = [P, ci, i64, i64, i64, i32, i32, i32, P, PP, u64, ci, ci, P, P, P, P]
     lib.ls_sample_speculative.restype = ci
-    lib.ls_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, P, P]
+    sz = ctypes.c_size_t
+    lib.ls_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, P, sz, P, P]
     lib.ls_log_probs.restype = ci
-    lib.ls_sample_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P, P, P]
+    lib.ls_log_probs_workspace_bytes.argtypes = [i32]
+    lib.ls_log_probs_workspace_bytes.restype = sz
+    lib.ls_sample_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P, P, sz, P, P]
     lib.ls_sample_log_probs.restype = ci
     lib.ls_sample_device_step.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, ci, ci, P, P, P]
     lib.ls_sample_device_step.restype = ci
@@ -224,8 +227,28 @@ def sample_speculative(required_logits, num_decode, num_prefill, num_speculative
     return out
 
 
+# Default of the log-prob calls' `workspace` argument (True: allocate one).
+LOG_PROBS_WORKSPACE = True
+
+
+def _workspace(lib, n, device, workspace):
+    """The log-prob calls' optional workspace: True allocates one (on the
+    current stream), False passes none (the row kernel then writes the rows
+    itself), None takes LOG_PROBS_WORKSPACE, or a caller's tensor.  Returns
+    (tensor or None, bytes)."""
+    import torch
+    if workspace is None:
+        workspace = LOG_PROBS_WORKSPACE
+    if workspace is False:
+        return None, 0
+    if workspace is True:
+        nbytes = int(lib.ls_log_probs_workspace_bytes(int(n)))
+        workspace = torch.empty(max(1, nbytes // 4), dtype=torch.float32, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
 def log_probs(logits, params, num_rows=None, gather_indices=None, token_to_request_index=None, out=None,
-              error_word=None, stream=None):
+              error_word=None, stream=None, workspace=None):
     """ls_log_probs: returns out (float32 [num_rows, vocab])."""
     import torch
     lib = load_library()
@@ -239,9 +262,10 @@ def log_probs(logits, params, num_rows=None, gather_indices=None, token_to_reque
         if out.dtype != torch.float32 or not out.is_contiguous() or out.numel() < num_rows * V:
             raise ValueError("out must be a contiguous float32 tensor of num_rows * vocab entries")
         prm = params.as_struct()
+        ws, wsb = _workspace(lib, num_rows, logits.device, workspace)
         st = lib.ls_log_probs(ptr, dt, rows, V, stride, int(num_rows), _i32(gather_indices, "gather_indices"),
                               _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
-                              _dptr(out), _i32(error_word, "error_word"), _stream(s))
+                              _dptr(out), _dptr(ws), wsb, _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_log_probs")
     return out
@@ -249,7 +273,7 @@ def log_probs(logits, params, num_rows=None, gather_indices=None, token_to_reque
 
 def sample_log_probs(logits, n, params, step, no_top_k, no_top_p, gather_indices=None, token_to_request_index=None,
                      want_log_probs=True, want_selected=True, out=None, out_log_probs=None, out_selected=None,
-                     error_word=None, stream=None):
+                     error_word=None, stream=None, workspace=None):
     """ls_sample_log_probs: returns (ids int32 [n], log_probs float32 [n, vocab] or None,
     selected float32 [n] or None) from one read of the logits."""
     import torch
@@ -273,11 +297,12 @@ def sample_log_probs(logits, n, params, step, no_top_k, no_top_p, gather_indices
         if out_selected is not None and (out_selected.dtype != torch.float32 or out_selected.numel() < n):
             raise ValueError("out_selected must be a float32 tensor of n entries")
         prm = params.as_struct()
+        ws, wsb = _workspace(lib, n, logits.device, workspace if out_log_probs is not None else False)
         st = lib.ls_sample_log_probs(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
                                      _i32(token_to_request_index, "token_to_request_index"), ctypes.byref(prm),
                                      int(step), int(bool(no_top_k)), int(bool(no_top_p)), _i32(out, "out"),
-                                     _dptr(out_log_probs), _dptr(out_selected), _i32(error_word, "error_word"),
-                                     _stream(s))
+                                     _dptr(out_log_probs), _dptr(out_selected), _dptr(ws), wsb,
+                                     _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_sample_log_probs")
     return out, out_log_probs, out_selected

@@ -44,6 +44,14 @@ enum MapMode { MAP_IDENTITY = 0, MAP_T2R = 1, MAP_SPEC = 2 };
 enum Mode { MODE_SAMPLE = 0, MODE_LOGPROBS = 1, MODE_BOTH = 2 };
 enum Route { ROUTE_NONE = 0, ROUTE_K = 1, ROUTE_P = 2, ROUTE_KP = 3 };
 
+// Scalars of a deferred log-prob row (the row kernel leaves them for
+// lp_write_kernel): kept = v >= lo; value = (v - M) / T - lnS for T > 0, the
+// constant -lnS for T == 0 (rows whose kept set is the maximum's ties); M NaN
+// marks an error row (NaN throughout).
+struct alignas(16) LpRow {
+  float M, T, lnS, lo;
+};
+
 struct KernelArgs {
   const void* logits;
   int64_t logits_rows, vocab, stride;
@@ -69,6 +77,7 @@ struct KernelArgs {
   int32_t gslot_cap;  // group-maximum slots of one CTA's slice (split sampler)
   int32_t ent_cap;    // capacity of the candidate-entry list (split sampler)
   int32_t pool_cap;   // captured-group slots shared by the warps once their own are full (split sampler)
+  LpRow* lp_rows;     // when not NULL the log-prob rows are written by lp_write_kernel from these
 };
 
 constexpr int kWarpList = 128;  // candidate groups a warp lists before loading them
@@ -837,8 +846,12 @@ __device__ __forceinline__ void row_error(const KernelArgs& a, int64_t i, int mo
     if (a.error_word) atomicOr(a.error_word, err);
   }
   if (mode == MODE_LOGPROBS || (mode == MODE_BOTH && a.out_lp)) {
-    float* out = a.out_lp + i * a.vocab;
     const float nan = __uint_as_float(0x7FC00000u);
+    if (a.lp_rows) {
+      if (threadIdx.x == 0) a.lp_rows[i] = LpRow{nan, 0.f, 0.f, 0.f};
+      return;
+    }
+    float* out = a.out_lp + i * a.vocab;
     for (int64_t j = threadIdx.x; j < a.vocab; j += kThreads) out[j] = nan;
   }
 }
@@ -849,54 +862,72 @@ __device__ __forceinline__ void st_stream4(float* p, float a, float b, float c, 
   asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-// Write out[j] = kept(v_j) ? value(v_j) : -inf over the whole row.  The row
-// is read again (normally from L2) group by group with the streaming pass's
-// 256-bit loads, one group per thread at a time (more groups in flight were
-// measured slower), and each group's 16 outputs go out four at a time as
-// 16-byte streaming stores when their start is 16-byte aligned (the same for
-// every group of a row), else one by one.
-template <typename TIn, typename KeptF, typename ValF>
-__device__ __forceinline__ void write_row(const RowView<TIn>& rv, float* out, KeptF kept, ValF val) {
-  using RVT = RowView<TIn>;
+// Whether a row's outputs can go out as 16-byte stores: its groups' first
+// entries land on 16-byte boundaries of `out` (the same for every group).
+template <typename TIn>
+__device__ __forceinline__ bool out_vec(const RowView<TIn>& rv, const float* out) {
   const uintptr_t oa = reinterpret_cast<uintptr_t>(out);
-  const bool vec = (oa & 3u) == 0u && (((oa >> 2) - (uintptr_t)rv.off) & 3u) == 0u;
-  constexpr int U = 1;
-  const uint64_t pol = l2_evict_first_policy();  // the row's last use
-  for (int g0 = threadIdx.x; g0 < rv.NG; g0 += U * kThreads) {
-    uint32_t w[U][RVT::kWords];
+  return (oa & 3u) == 0u && (((oa >> 2) - (uintptr_t)rv.off) & 3u) == 0u;
+}
+
+// out[j] = kept(v_j) ? value(v_j) : -inf for the 16 entries of group g (words
+// w, loaded already unless the group is ragged), four at a time as 16-byte
+// streaming stores when vec, else one by one.
+template <typename TIn, typename KeptF, typename ValF>
+__device__ __forceinline__ void write_group(const RowView<TIn>& rv, float* out, bool vec, int g,
+                                            uint32_t (&w)[RowView<TIn>::kWords], KeptF kept, ValF val) {
+  using RVT = RowView<TIn>;
+  const bool full = rv.full(g);
+  if (!full) rv.load_words_partial(g, w);
+  const int64_t j0 = rv.index(g, 0);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int g = g0 + u * kThreads;
-      if (g < rv.NG && rv.full(g)) rv.load_words(g, w[u], pol);
+  for (int h = 0; h < kGroup / 4; ++h) {
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float v = RVT::element_at(w, 4 * h + e);
+      o[e] = kept(v) ? val(v) : kNegInf;
     }
+    if (vec && full) {
+      st_stream4(out + j0 + 4 * h, o[0], o[1], o[2], o[3]);
+    } else {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int g = g0 + u * kThreads;
-      if (g < rv.NG) {
-        const bool full = rv.full(g);
-        if (!full) rv.load_words_partial(g, w[u]);
-        const int64_t j0 = rv.index(g, 0);
-#pragma unroll
-        for (int h = 0; h < kGroup / 4; ++h) {
-          float o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v = RVT::element_at(w[u], 4 * h + e);
-            o[e] = kept(v) ? val(v) : kNegInf;
-          }
-          if (vec && full) {
-            st_stream4(out + j0 + 4 * h, o[0], o[1], o[2], o[3]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int64_t j = j0 + 4 * h + e;
-              if (j >= 0 && j < rv.V) out[j] = o[e];
-            }
-          }
-        }
+      for (int e = 0; e < 4; ++e) {
+        const int64_t j = j0 + 4 * h + e;
+        if (j >= 0 && j < rv.V) out[j] = o[e];
       }
     }
   }
+}
+
+// Write out[j] = kept(v_j) ? value(v_j) : -inf over the whole row.  The row
+// is read again (normally from L2) group by group with the streaming pass's
+// 256-bit loads, one group per thread at a time (more groups in flight were
+// measured slower).
+template <typename TIn, typename KeptF, typename ValF>
+__device__ __forceinline__ void write_row(const RowView<TIn>& rv, float* out, KeptF kept, ValF val) {
+  const bool vec = out_vec(rv, out);
+  const uint64_t pol = l2_evict_first_policy();  // the row's last use
+  for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
+    uint32_t w[RowView<TIn>::kWords];
+    if (rv.full(g)) rv.load_words(g, w, pol);
+    write_group(rv, out, vec, g, w, kept, val);
+  }
+}
+
+// Value of a kept entry of a log-prob row: (v - M) / T - lnS, the division a
+// multiplication by RN(1/T) while |(v - M) / T| < 256 (an error below
+// 3 2^-24 256 + half an ulp of the result, inside the 1e-4 the log-probs are
+// held to), the correctly rounded division beyond.
+struct LpValue {
+  float M, T, lnS, invT, lim;
+  __device__ __forceinline__ float operator()(float v) const {
+    const float d = v - M;
+    return (fabsf(d) < lim ? d * invT : __fdiv_rn(d, T)) - lnS;
+  }
+};
+__device__ __forceinline__ LpValue lp_value(float M, float T, float lnS) {
+  return LpValue{M, T, lnS, __frcp_rn(T), 256.f * T};
 }
 
 template <typename TIn, int ROUTE, int MODE>
@@ -1333,7 +1364,11 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     }
     if (want_lp) {
       const float lp = -logf((float)sh.acc[0]);
-      write_row(rv, a.out_lp + i * V, [&](float v) { return v >= M; }, [&](float) { return lp; });
+      if (a.lp_rows) {
+        if (tid == 0) a.lp_rows[i] = LpRow{M, 0.f, -lp, M};
+      } else {
+        write_row(rv, a.out_lp + i * V, [&](float v) { return v >= M; }, [&](float) { return lp; });
+      }
     }
     return;
   }
@@ -1392,15 +1427,11 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     // The masses are 2^(v c - R) = exp((v - M) / T) * 2^(M c - R); remove the
     // exactly computable residual of R's rounding from the normaliser.
     lnS -= fmaf(M, c, -R) * 0.6931471805599453f;
-    // (v - M) / T: a multiplication by RN(1/T) while |(v - M) / T| < 256 (an
-    // error below 3 2^-24 256 + half an ulp of the result, inside the 1e-4
-    // the log-probs are held to), the correctly rounded division beyond
-    const float invT = __frcp_rn(T), lim = 256.f * T;
-    write_row(rv, a.out_lp + i * V, [&](float v) { return v >= lo_val; },
-              [&](float v) {
-                const float d = v - M;
-                return (fabsf(d) < lim ? d * invT : __fdiv_rn(d, T)) - lnS;
-              });
+    if (a.lp_rows) {
+      if (tid == 0) a.lp_rows[i] = LpRow{M, T, lnS, lo_val};
+    } else {
+      write_row(rv, a.out_lp + i * V, [&](float v) { return v >= lo_val; }, lp_value(M, T, lnS));
+    }
   }
 }
 
@@ -1467,6 +1498,10 @@ static ls_status launch_rows(const KernelArgs& a, int32_t n, size_t smem, cudaSt
   if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return LS_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? LS_OK : LS_ERR_CUDA;
 }
+
+// The deferred log-prob write (ls_lpwrite.cu): every row's log-probs from
+// the LpRow scalars the row kernel left in a.lp_rows, tiled over all SMs.
+ls_status dispatch_lp_write(const KernelArgs& a, ls_dtype dtype, int32_t n, cudaStream_t stream);
 
 template <int MODE>
 ls_status dispatch(KernelArgs a, ls_dtype dtype, int route, int32_t n, cudaStream_t stream) {

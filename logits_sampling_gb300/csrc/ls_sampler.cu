@@ -70,6 +70,32 @@ ls_status dispatch_sample(const KernelArgs& a, ls_dtype dtype, int route, int32_
   }
 }
 
+// L2 size of the current device in bytes (cached per device), 0 if unknown.
+static int64_t l2_bytes() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices && (v = cache[dev].load(std::memory_order_relaxed)) > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Whether a log-prob call with a workspace writes its rows through
+// lp_write_kernel: the batch's logits fit in 60% of L2, so the write finds
+// them there (a larger batch keeps the row kernel's own write, which re-reads
+// each row right after its streaming pass).
+static bool lp_deferred(int32_t n, int64_t vocab, ls_dtype dtype) {
+  const int64_t l2 = l2_bytes();
+  const int64_t bytes = (int64_t)n * vocab * (dtype == LS_DTYPE_BF16 ? 2 : 4);
+  return l2 > 0 && bytes * 5 <= l2 * 3;
+}
+
+// A workspace is absent, or large enough and 16-byte aligned.
+static bool workspace_ok(const void* ws, size_t bytes, int32_t n) {
+  return !ws || (bytes >= (size_t)n * sizeof(LpRow) && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0u);
+}
+
 // Advances a device-resident Philox step word after the sampler that read it
 // (stream order: every CTA of the sampler has read the word before this runs).
 __global__ void advance_step_kernel(uint64_t* step) { *step += 1ull; }
@@ -125,12 +151,18 @@ ls_status ls_sample_speculative(const void* required_logits, ls_dtype dtype, int
   return dispatch_sample(a, dtype, route, n, static_cast<cudaStream_t>(stream));
 }
 
+size_t ls_log_probs_workspace_bytes(int32_t num_rows) {
+  return num_rows > 0 ? (size_t)num_rows * sizeof(LpRow) : 0u;
+}
+
 ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab, int64_t row_stride,
                        int32_t num_rows, const int32_t* gather_indices, const int32_t* token_to_request_index,
-                       const ls_params* params, float* out_log_probs, int32_t* error_word, void* stream) {
+                       const ls_params* params, float* out_log_probs, void* workspace, size_t workspace_bytes,
+                       int32_t* error_word, void* stream) {
   if (num_rows < 0) return LS_ERR_INVALID_ARG;
   if (num_rows == 0) return LS_OK;
-  if (!common_ok(logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, false) || !out_log_probs)
+  if (!common_ok(logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, false) || !out_log_probs ||
+      !workspace_ok(workspace, workspace_bytes, num_rows))
     return LS_ERR_INVALID_ARG;
   if (!gather_indices && (int64_t)num_rows > logits_rows) return LS_ERR_INVALID_ARG;
   if (!token_to_request_index && num_rows > params->num_requests) return LS_ERR_INVALID_ARG;
@@ -138,7 +170,11 @@ ls_status ls_log_probs(const void* logits, ls_dtype dtype, int64_t logits_rows, 
   a.t2r = token_to_request_index;
   a.map_mode = token_to_request_index ? MAP_T2R : MAP_IDENTITY;
   a.out_lp = out_log_probs;
-  return dispatch<MODE_LOGPROBS>(a, dtype, ROUTE_KP, num_rows, static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (workspace && lp_deferred(num_rows, vocab, dtype)) a.lp_rows = static_cast<LpRow*>(workspace);
+  const ls_status rc = dispatch<MODE_LOGPROBS>(a, dtype, ROUTE_KP, num_rows, st);
+  if (rc != LS_OK || !a.lp_rows) return rc;
+  return dispatch_lp_write(a, dtype, num_rows, st);
 }
 
 ls_status ls_sample_device_step(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
@@ -168,10 +204,12 @@ ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits
                               int64_t row_stride, int32_t n, const int32_t* gather_indices,
                               const int32_t* token_to_request_index, const ls_params* params, uint64_t step,
                               int no_top_k, int no_top_p, int32_t* out_ids, float* out_log_probs,
-                              float* out_selected_log_probs, int32_t* error_word, void* stream) {
+                              float* out_selected_log_probs, void* workspace, size_t workspace_bytes,
+                              int32_t* error_word, void* stream) {
   if (n < 0) return LS_ERR_INVALID_ARG;
   if (n == 0) return LS_OK;
-  if (!common_ok(logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, true) || !out_ids)
+  if (!common_ok(logits, dtype, logits_rows, vocab, row_stride) || !params_ok(params, true) || !out_ids ||
+      !workspace_ok(workspace, workspace_bytes, n))
     return LS_ERR_INVALID_ARG;
   if (!gather_indices && (int64_t)n > logits_rows) return LS_ERR_INVALID_ARG;
   if (!token_to_request_index && n > params->num_requests) return LS_ERR_INVALID_ARG;
@@ -182,9 +220,13 @@ ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits
   a.out_lp = out_log_probs;
   a.out_sel = out_selected_log_probs;
   const int route = (no_top_k ? 0 : ROUTE_K) | (no_top_p ? 0 : ROUTE_P);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (!out_log_probs && !out_selected_log_probs)  // ids only: the sampling kernels
-    return dispatch_sample(a, dtype, route, n, static_cast<cudaStream_t>(stream));
-  return dispatch<MODE_BOTH>(a, dtype, route, n, static_cast<cudaStream_t>(stream));
+    return dispatch_sample(a, dtype, route, n, st);
+  if (out_log_probs && workspace && lp_deferred(n, vocab, dtype)) a.lp_rows = static_cast<LpRow*>(workspace);
+  const ls_status rc = dispatch<MODE_BOTH>(a, dtype, route, n, st);
+  if (rc != LS_OK || !a.lp_rows) return rc;
+  return dispatch_lp_write(a, dtype, n, st);
 }
 
 int ls_set_split_policy(int ctas_per_row) {

@@ -40,3 +40,13 @@ def split_policy(request):
     ls.set_split_policy(request.param)
     yield request.param
     ls.set_split_policy(0)
+
+
+@pytest.fixture(params=[True, False], ids=["tiled-write", "row-write"])
+def lp_write(request):
+    """Log-prob calls with a workspace (rows whose logits fit in L2 are written
+    by the tiled write kernel) and without (the row kernel writes each row)."""
+    from logits_sampling_gb300 import _binding
+    _binding.LOG_PROBS_WORKSPACE = request.param
+    yield request.param
+    _binding.LOG_PROBS_WORKSPACE = True

@@ -88,16 +88,22 @@ def test_host_validation_before_any_launch(lib):
     assert lib.ls_sample_speculative(fake, 1, 100, 10, 10, 0, 0, 3, None, byref(prm), 0, 0, 0, fake, None, None,
                                      None) == 0
     # log-probs
-    assert lib.ls_log_probs(fake, 1, 4, 10, 10, -2, None, None, byref(prm), fake, None, None) == 1
-    assert lib.ls_log_probs(fake, 1, 4, 10, 10, 0, None, None, byref(prm), fake, None, None) == 0
-    assert lib.ls_log_probs(fake, 1, 4, 10, 10, 2, None, None, byref(prm), None, None, None) == 1
+    lp = lib.ls_log_probs
+    assert lp(fake, 1, 4, 10, 10, -2, None, None, byref(prm), fake, None, 0, None, None) == 1
+    assert lp(fake, 1, 4, 10, 10, 0, None, None, byref(prm), fake, None, 0, None, None) == 0
+    assert lp(fake, 1, 4, 10, 10, 2, None, None, byref(prm), None, None, 0, None, None) == 1
+    # the optional workspace: 16 bytes per row, 16-byte aligned
+    assert lib.ls_log_probs_workspace_bytes(3) == 48 and lib.ls_log_probs_workspace_bytes(0) == 0
+    assert lp(fake, 1, 4, 10, 10, 2, None, None, byref(prm), fake, fake, 31, None, None) == 1
+    assert lp(fake, 1, 4, 10, 10, 2, None, None, byref(prm), fake, P(0x1008), 32, None, None) == 1
     # fused sample + log-probs: the ls_sample checks, and out_ids is required
     f = lib.ls_sample_log_probs
-    assert f(fake, 1, 4, 10, 10, -1, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, None) == 1
-    assert f(fake, 1, 4, 10, 10, 0, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, None) == 0
-    assert f(fake, 1, 4, 10, 10, 2, None, None, byref(prm), 0, 0, 0, None, fake, fake, None, None) == 1
-    assert f(fake, 1, 4, 10, 10, 5, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, None) == 1
-    assert f(fake, 1, 4, 10, 10, 3, None, None, byref(prm2), 0, 0, 0, fake, None, fake, None, None) == 1
+    assert f(fake, 1, 4, 10, 10, -1, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, 0, None, None) == 1
+    assert f(fake, 1, 4, 10, 10, 0, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, 0, None, None) == 0
+    assert f(fake, 1, 4, 10, 10, 2, None, None, byref(prm), 0, 0, 0, None, fake, fake, None, 0, None, None) == 1
+    assert f(fake, 1, 4, 10, 10, 5, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, 0, None, None) == 1
+    assert f(fake, 1, 4, 10, 10, 3, None, None, byref(prm2), 0, 0, 0, fake, None, fake, None, 0, None, None) == 1
+    assert f(fake, 1, 4, 10, 10, 2, None, None, byref(prm), 0, 0, 0, fake, fake, fake, fake, 16, None, None) == 1
     # device step word: the ls_sample checks, and the step pointer is required
     d = lib.ls_sample_device_step
     assert d(fake, 1, 4, 10, 10, 2, None, None, byref(prm), None, 0, 0, fake, None, None) == 1

@@ -10,7 +10,7 @@ from logits_sampling_gb300 import workloads as W
 from gpu_util import check_ids, check_log_probs
 
 # every test runs under each kernel choice of the sampling calls
-pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("split_policy")]
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("split_policy", "lp_write")]
 
 
 @pytest.fixture(scope="module", autouse=True)

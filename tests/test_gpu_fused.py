@@ -9,7 +9,7 @@ from logits_sampling_gb300 import workloads as W
 
 from gpu_util import check_ids, check_log_probs, odt, params_of, selected_tolerance, to_device
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("lp_write")]
 
 
 @pytest.fixture(scope="module", autouse=True)

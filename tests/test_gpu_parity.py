@@ -40,6 +40,7 @@ def _lp_oracle(w, rows=None):
 # ---------------------------------------------------------------------------
 # the five workloads
 # ---------------------------------------------------------------------------
+@pytest.mark.usefixtures("lp_write")
 def test_tiny_ids_and_log_probs():
     w = W.make_tiny()
     ids, err, _ = gpu_sample(w)
@@ -52,6 +53,7 @@ def test_tiny_ids_and_log_probs():
     check_log_probs(lp, r, "tiny lp")
 
 
+@pytest.mark.usefixtures("lp_write")
 def test_decode_ids_and_log_probs():
     w = W.make_decode()
     ids, err, _ = gpu_sample(w)
@@ -69,6 +71,7 @@ def test_top_p_full_size_ids():
     check_ids(ids, oracle_sample(w), "top_p")
 
 
+@pytest.mark.usefixtures("lp_write")
 def test_top_p_log_probs_sampled_rows():
     w = W.make_top_p(rows=24)
     r, g, t, n = _lp_oracle(w)
@@ -84,6 +87,7 @@ def test_speculative_full_size_ids_and_mapping():
     check_ids(ids, oracle_sample(w), "speculative")
 
 
+@pytest.mark.usefixtures("lp_write")
 def test_speculative_log_probs_sampled_rows():
     w = W.make_speculative()
     rows = np.r_[0:5, 317:322, 638:642, 667:672]
@@ -101,6 +105,7 @@ def test_large_full_size_ids():
     assert nflag < 20
 
 
+@pytest.mark.usefixtures("lp_write")
 def test_large_log_probs_sampled_rows():
     w = W.make_large(rows=64, vocab=262144)
     r, g, t, n = _lp_oracle(w)
@@ -149,6 +154,7 @@ def test_steps_reproducible_and_fresh():
     check_ids(d, oracle_sample(w, step=big), "step 2^40+5")
 
 
+@pytest.mark.usefixtures("lp_write")
 def test_log_probs_deterministic():
     w = W.make_decode(rows=16, vocab=6000)
     a, _ = gpu_log_probs(w)
