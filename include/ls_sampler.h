@@ -223,6 +223,29 @@ ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits
                               float* out_selected_log_probs, void* workspace, size_t workspace_bytes,
                               int32_t* error_word, void* stream);
 
+/* Rows ls_sample_log_probs_noalloc accepts (its fixed scratch: 16 bytes per row). */
+#define LS_NOALLOC_MAX_ROWS 4096
+
+/*
+ * ls_sample_log_probs_noalloc -- ls_sample_log_probs without a caller
+ * workspace and without any allocation: the per-row scalars of the tiled
+ * log-prob write go to a fixed device array of this library
+ * (LS_NOALLOC_MAX_ROWS rows, 64 KB, located once per device).
+ *
+ * Results are exactly those of ls_sample_log_probs with a workspace.  n above
+ * LS_NOALLOC_MAX_ROWS returns LS_ERR_UNSUPPORTED with nothing launched.  Calls
+ * in flight at the same time on one device (other streams, other host
+ * threads) share that array and race; issue them one after another on one
+ * stream.  Nothing in the array has to start at zero.
+ * Arguments as for ls_sample_log_probs, without workspace and workspace_bytes.
+ */
+ls_status ls_sample_log_probs_noalloc(const void* logits, ls_dtype dtype, int64_t logits_rows, int64_t vocab,
+                                      int64_t row_stride, int32_t n, const int32_t* gather_indices,
+                                      const int32_t* token_to_request_index, const ls_params* params,
+                                      uint64_t step, int no_top_k, int no_top_p, int32_t* out_ids,
+                                      float* out_log_probs, float* out_selected_log_probs, int32_t* error_word,
+                                      void* stream);
+
 /*
  * ls_argmax -- the all-greedy fast path: out_ids[i] = the lowest index of the
  * maximum of logits row i (row gather_indices[i] when given).

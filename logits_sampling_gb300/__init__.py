@@ -3,8 +3,8 @@
 The binding only marshals arguments (torch tensors -> device pointers, the
 current CUDA stream) and calls the C ABI declared in include/ls_sampler.h:
 ``ls_sample``, ``ls_sample_speculative``, ``ls_log_probs``,
-``ls_sample_log_probs``, ``ls_sample_device_step``, ``ls_argmax``,
-``ls_verify_chain``, ``ls_sample_verify`` and ``ls_set_split_policy``.  Every step of the
+``ls_sample_log_probs``, ``ls_sample_log_probs_noalloc``, ``ls_sample_device_step``,
+``ls_argmax``, ``ls_verify_chain``, ``ls_sample_verify`` and ``ls_set_split_policy``.  Every step of the
 sampling path runs in the library's CUDA kernels; there is no CPU fallback.
 If the library has not been built (``python -m logits_sampling_gb300.build``)
 or no CUDA device is present, the calls raise.
@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     LS_ROW_ERR_BAD_GATHER,
     LS_ROW_ERR_BAD_REQUEST,
     LS_ROW_ERR_NO_FINITE,
+    NOALLOC_MAX_ROWS,
     LSError,
     SamplingParams,
     argmax,
@@ -25,6 +26,7 @@ from ._binding import (  # noqa: F401
     sample,
     sample_device_step,
     sample_log_probs,
+    sample_log_probs_noalloc,
     sample_speculative,
     sample_verify,
     set_split_policy,

@@ -57,6 +57,8 @@ def configure(lib):
     lib.ls_log_probs_workspace_bytes.restype = sz
     lib.ls_sample_log_probs.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P, P, sz, P, P]
     lib.ls_sample_log_probs.restype = ci
+    lib.ls_sample_log_probs_noalloc.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P, P, P]
+    lib.ls_sample_log_probs_noalloc.restype = ci
     lib.ls_sample_device_step.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, ci, ci, P, P, P]
     lib.ls_sample_device_step.restype = ci
     lib.ls_argmax.argtypes = [P, ci, i64, i64, i64, i32, P, P, P, P]
@@ -227,6 +229,9 @@ def sample_speculative(required_logits, num_decode, num_prefill, num_speculative
     return out
 
 
+# Rows of ls_sample_log_probs_noalloc's fixed scratch (LS_NOALLOC_MAX_ROWS).
+NOALLOC_MAX_ROWS = 4096
+
 # Default of the log-prob calls' `workspace` argument (True: allocate one).
 LOG_PROBS_WORKSPACE = True
 
@@ -305,6 +310,35 @@ def sample_log_probs(logits, n, params, step, no_top_k, no_top_p, gather_indices
                                      _i32(error_word, "error_word"), _stream(s))
     if st != LS_OK:
         raise LSError(st, "ls_sample_log_probs")
+    return out, out_log_probs, out_selected
+
+
+def sample_log_probs_noalloc(logits, n, params, step, no_top_k, no_top_p, gather_indices=None,
+                             token_to_request_index=None, out=None, out_log_probs=None, out_selected=None,
+                             error_word=None, stream=None):
+    """ls_sample_log_probs_noalloc: as sample_log_probs with both outputs,
+    the outputs given or allocated here; the library's fixed scratch replaces
+    the workspace (n at most LS_NOALLOC_MAX_ROWS; calls in flight together
+    race on it)."""
+    import torch
+    lib = load_library()
+    ptr, dt, rows, V, stride = _logits_desc(logits)
+    s, ctx = _on(stream)
+    with ctx:
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device=logits.device)
+        if out_log_probs is None:
+            out_log_probs = torch.empty((n, V), dtype=torch.float32, device=logits.device)
+        if out_selected is None:
+            out_selected = torch.empty(n, dtype=torch.float32, device=logits.device)
+        prm = params.as_struct()
+        st = lib.ls_sample_log_probs_noalloc(ptr, dt, rows, V, stride, int(n), _i32(gather_indices, "gather_indices"),
+                                             _i32(token_to_request_index, "token_to_request_index"),
+                                             ctypes.byref(prm), int(step), int(bool(no_top_k)), int(bool(no_top_p)),
+                                             _i32(out, "out"), _dptr(out_log_probs), _dptr(out_selected),
+                                             _i32(error_word, "error_word"), _stream(s))
+    if st != LS_OK:
+        raise LSError(st, f"ls_sample_log_probs_noalloc (n = {n}; at most {NOALLOC_MAX_ROWS} rows)")
     return out, out_log_probs, out_selected
 
 

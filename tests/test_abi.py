@@ -104,6 +104,11 @@ def test_host_validation_before_any_launch(lib):
     assert f(fake, 1, 4, 10, 10, 5, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, 0, None, None) == 1
     assert f(fake, 1, 4, 10, 10, 3, None, None, byref(prm2), 0, 0, 0, fake, None, fake, None, 0, None, None) == 1
     assert f(fake, 1, 4, 10, 10, 2, None, None, byref(prm), 0, 0, 0, fake, fake, fake, fake, 16, None, None) == 1
+    # the fixed-scratch fused call: more rows than its scratch are refused
+    # before any CUDA call; n == 0 launches nothing
+    nf = lib.ls_sample_log_probs_noalloc
+    assert nf(fake, 1, 5000, 10, 10, 4097, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, None) == 2
+    assert nf(fake, 1, 4, 10, 10, 0, None, None, byref(prm), 0, 0, 0, fake, fake, fake, None, None) == 0
     # device step word: the ls_sample checks, and the step pointer is required
     d = lib.ls_sample_device_step
     assert d(fake, 1, 4, 10, 10, 2, None, None, byref(prm), None, 0, 0, fake, None, None) == 1
