@@ -862,6 +862,23 @@ __device__ __forceinline__ void st_stream4(float* p, float a, float b, float c, 
   asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+// 8- or 16-byte load of four consecutive logits (no L1 allocation, an L2
+// eviction policy).
+__device__ __forceinline__ void ld_quad(const void* p, uint32_t (&r)[2], uint64_t pol) {
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+               : "=r"(r[0]), "=r"(r[1])
+               : "l"(p), "l"(pol));
+}
+__device__ __forceinline__ void ld_quad(const void* p, uint32_t (&r)[4], uint64_t pol) {
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "l"(p), "l"(pol));
+}
+__device__ __forceinline__ float quad_at(const uint32_t (&r)[2], int e) {
+  return __uint_as_float((e & 1) ? (r[e >> 1] & 0xFFFF0000u) : (r[e >> 1] << 16));
+}
+__device__ __forceinline__ float quad_at(const uint32_t (&r)[4], int e) { return __uint_as_float(r[e]); }
+
 // Whether a row's outputs can go out as 16-byte stores: its groups' first
 // entries land on 16-byte boundaries of `out` (the same for every group).
 template <typename TIn>
@@ -900,16 +917,51 @@ __device__ __forceinline__ void write_group(const RowView<TIn>& rv, float* out, 
   }
 }
 
-// Write out[j] = kept(v_j) ? value(v_j) : -inf over the whole row.  The row
-// is read again (normally from L2) group by group with the streaming pass's
-// 256-bit loads, one group per thread at a time (more groups in flight were
-// measured slower).
+// Write out[j] = kept(v_j) ? value(v_j) : -inf over the whole row, reading
+// the row again (normally from L2).  When the row and the output allow it,
+// entries go four at a time: a warp's loads and 16-byte streaming stores
+// cover consecutive addresses (kWriteQuads quads of a thread in flight
+// together); otherwise group by group with the streaming pass's 256-bit loads.
+constexpr int kWriteQuads = 4;
 template <typename TIn, typename KeptF, typename ValF>
 __device__ __forceinline__ void write_row(const RowView<TIn>& rv, float* out, KeptF kept, ValF val) {
-  const bool vec = out_vec(rv, out);
+  using RVT = RowView<TIn>;
+  constexpr int E = RVT::kBytes;
+  constexpr int QW = E == 2 ? 2 : 4;
   const uint64_t pol = l2_evict_first_policy();  // the row's last use
+  const int64_t V = rv.V;
+  if ((reinterpret_cast<uintptr_t>(rv.row) & (4 * E - 1)) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    const int64_t nq = V / 4;  // whole quads; the last 1-3 entries one by one
+    for (int64_t q0 = threadIdx.x; q0 < nq; q0 += (int64_t)kWriteQuads * kThreads) {
+      uint32_t w[kWriteQuads][QW];
+#pragma unroll
+      for (int u = 0; u < kWriteQuads; ++u) {
+        const int64_t q = q0 + (int64_t)u * kThreads;
+        if (q < nq) ld_quad(rv.row + 4 * q, w[u], pol);
+      }
+#pragma unroll
+      for (int u = 0; u < kWriteQuads; ++u) {
+        const int64_t q = q0 + (int64_t)u * kThreads;
+        if (q < nq) {
+          float o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v = quad_at(w[u], e);
+            o[e] = kept(v) ? val(v) : kNegInf;
+          }
+          st_stream4(out + 4 * q, o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    for (int64_t j = 4 * nq + threadIdx.x; j < V; j += kThreads) {
+      const float v = rv.at(j);
+      out[j] = kept(v) ? val(v) : kNegInf;
+    }
+    return;
+  }
+  const bool vec = out_vec(rv, out);
   for (int g = threadIdx.x; g < rv.NG; g += kThreads) {
-    uint32_t w[RowView<TIn>::kWords];
+    uint32_t w[RVT::kWords];
     if (rv.full(g)) rv.load_words(g, w, pol);
     write_group(rv, out, vec, g, w, kept, val);
   }

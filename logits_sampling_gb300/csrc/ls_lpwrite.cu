@@ -19,23 +19,6 @@ constexpr int kLpTileEntries = 8192;
 constexpr int kLpQuads = kLpTileEntries / 4 / kLpThreads;     // quads of 4 entries per thread and tile
 constexpr int kLpPer = kLpTileEntries / kGroup / kLpThreads;  // groups per thread and tile (unaligned rows)
 
-// 8- or 16-byte load of four consecutive logits (no L1 allocation, an L2
-// eviction policy).
-__device__ __forceinline__ void ld_quad(const void* p, uint32_t (&r)[2], uint64_t pol) {
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
-               : "=r"(r[0]), "=r"(r[1])
-               : "l"(p), "l"(pol));
-}
-__device__ __forceinline__ void ld_quad(const void* p, uint32_t (&r)[4], uint64_t pol) {
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "l"(p), "l"(pol));
-}
-__device__ __forceinline__ float quad_at(const uint32_t (&r)[2], int e) {
-  return __uint_as_float((e & 1) ? (r[e >> 1] & 0xFFFF0000u) : (r[e >> 1] << 16));
-}
-__device__ __forceinline__ float quad_at(const uint32_t (&r)[4], int e) { return __uint_as_float(r[e]); }
-
 template <typename TIn>
 __global__ void __launch_bounds__(kLpThreads) lp_write_kernel(const KernelArgs a, int tiles) {
   using RVT = RowView<TIn>;
