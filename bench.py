@@ -393,11 +393,13 @@ def run_ours(args, world, rank, local):
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     traffic = ncu_traffic(traffic_key(args.workload, args.call, args.route, args.split))
     # kernels launched per step: the log-prob calls add the tiled write kernel
-    # when the batch's logits fit in 60% of L2 (the library's rule)
+    # for batches of at most 3/4 of the SM count of rows, of at least 16384
+    # entries, whose logits fit in 60% of L2 (the library's rule)
     per_step = {"sample": 1, "argmax": 1, "verify": 2}.get(args.call)
     if per_step is None:
-        l2 = torch.cuda.get_device_properties(device).L2_cache_size
-        deferred = w.n * w.vocab * x.element_size() * 5 <= l2 * 3
+        props = torch.cuda.get_device_properties(device)
+        deferred = (w.n * 4 <= props.multi_processor_count * 3 and w.vocab >= 16384
+                    and w.n * w.vocab * x.element_size() * 5 <= props.L2_cache_size * 3)
         per_step = (1 if args.call == "fused" else 2) + (1 if deferred else 0)
     line = {
         "metric": METRIC, "value": rows_per_s, "unit": "rows/s", "n_gpus": world, "steps": args.steps,

@@ -150,11 +150,13 @@ ls_status ls_sample_speculative(const void* required_logits, ls_dtype dtype, int
  *                   ls_log_probs_workspace_bytes(num_rows) bytes, 16-byte
  *                   aligned, owned by the caller and not used by other calls
  *                   in flight (otherwise LS_ERR_INVALID_ARG).  With a
- *                   workspace, a batch whose logits fit in 60% of L2 takes two
- *                   launches: the row kernel leaves 16 bytes of scalars per row
- *                   there, and a second kernel writes the rows in tiles spread
- *                   over every SM (the same values).  Without one, or for a
- *                   larger batch, the row kernel writes each row itself.
+ *                   workspace, a batch of at most 3/4 of the SM count of rows,
+ *                   of at least 16384 entries each, whose logits fit in 60% of
+ *                   L2, takes two launches: the row kernel leaves 16 bytes of
+ *                   scalars per row there, and a second kernel writes the rows
+ *                   in tiles spread over every SM (the same values;
+ *                   ls_set_log_prob_write_policy overrides the choice).
+ *                   Otherwise the row kernel writes each row itself.
  *   workspace_bytes size of workspace (ignored when it is NULL)
  * Other arguments as for ls_sample.
  */
@@ -329,6 +331,18 @@ ls_status ls_sample_verify(const void* logits, ls_dtype dtype, int64_t logits_ro
  * Not synchronised with calls in flight on other host threads.
  */
 int ls_set_split_policy(int ctas_per_row);
+
+/*
+ * ls_set_log_prob_write_policy -- which write the log-prob calls given a
+ * workspace take, for every later call in the process (tests and tuning; both
+ * write the same values):
+ *   0   chosen from the batch shape (default; see ls_log_probs)
+ *   1   the tiled write kernel
+ *   -1  the row kernel's own write pass
+ * Returns LS_OK, or LS_ERR_INVALID_ARG for any other value (unchanged).
+ * Not synchronised with calls in flight on other host threads.
+ */
+int ls_set_log_prob_write_policy(int policy);
 
 /* Human-readable name of a status code (static storage). */
 const char* ls_status_string(ls_status s);

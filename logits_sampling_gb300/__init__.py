@@ -4,7 +4,8 @@ The binding only marshals arguments (torch tensors -> device pointers, the
 current CUDA stream) and calls the C ABI declared in include/ls_sampler.h:
 ``ls_sample``, ``ls_sample_speculative``, ``ls_log_probs``,
 ``ls_sample_log_probs``, ``ls_sample_log_probs_noalloc``, ``ls_sample_device_step``,
-``ls_argmax``, ``ls_verify_chain``, ``ls_sample_verify`` and ``ls_set_split_policy``.  Every step of the
+``ls_argmax``, ``ls_verify_chain``, ``ls_sample_verify``, ``ls_set_split_policy`` and
+``ls_set_log_prob_write_policy``.  Every step of the
 sampling path runs in the library's CUDA kernels; there is no CPU fallback.
 If the library has not been built (``python -m logits_sampling_gb300.build``)
 or no CUDA device is present, the calls raise.
@@ -29,6 +30,7 @@ from ._binding import (  # noqa: F401
     sample_log_probs_noalloc,
     sample_speculative,
     sample_verify,
+    set_log_prob_write_policy,
     set_split_policy,
     status_string,
     verify_chain,

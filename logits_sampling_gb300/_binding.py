@@ -59,6 +59,8 @@ def configure(lib):
     lib.ls_sample_log_probs.restype = ci
     lib.ls_sample_log_probs_noalloc.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, u64, ci, ci, P, P, P, P, P]
     lib.ls_sample_log_probs_noalloc.restype = ci
+    lib.ls_set_log_prob_write_policy.argtypes = [ci]
+    lib.ls_set_log_prob_write_policy.restype = ci
     lib.ls_sample_device_step.argtypes = [P, ci, i64, i64, i64, i32, P, P, PP, P, ci, ci, P, P, P]
     lib.ls_sample_device_step.restype = ci
     lib.ls_argmax.argtypes = [P, ci, i64, i64, i64, i32, P, P, P, P]
@@ -85,6 +87,14 @@ def status_string(status):
 
 def max_vocab(dtype=LS_DTYPE_BF16):
     return int(load_library().ls_max_vocab(dtype))
+
+
+def set_log_prob_write_policy(policy):
+    """ls_set_log_prob_write_policy: 0 from the batch shape, 1 the tiled write
+    kernel, -1 the row kernel's own write (calls with a workspace)."""
+    st = load_library().ls_set_log_prob_write_policy(int(policy))
+    if st != LS_OK:
+        raise LSError(st, f"ls_set_log_prob_write_policy({policy})")
 
 
 def set_split_policy(ctas_per_row):

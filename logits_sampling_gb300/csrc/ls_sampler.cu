@@ -81,14 +81,27 @@ static int64_t l2_bytes() {
   return v;
 }
 
+// Which write the log-prob calls with a workspace take
+// (ls_set_log_prob_write_policy): 0 = from the batch shape; 1 = the tiled
+// write kernel; -1 = the row kernel's own write pass.
+static std::atomic<int> g_lp_write_policy{0};
+
 // Whether a log-prob call with a workspace writes its rows through
-// lp_write_kernel: the batch's logits fit in 60% of L2, so the write finds
-// them there (a larger batch keeps the row kernel's own write, which re-reads
-// each row right after its streaming pass).
+// lp_write_kernel.  Measured on top_p-shaped rows (bf16, 128256 entries): the
+// tiled write wins while the batch leaves SMs idle (8 rows: 20.5 against
+// 28.7 us; 96 rows: 27.9 against 30.9) and loses once every SM holds a row
+// (152 rows: 35.9 against 33.0; 256 rows: 52.1 against 49.3), because the row
+// kernel then overlaps its early rows' writes with the other rows' streaming.
+// So: at most 3/4 of the SM count of rows, rows of at least 16384 entries
+// (shorter rows write faster than a second launch costs), and logits that
+// fit in 60% of L2 (the write finds them there).
 static bool lp_deferred(int32_t n, int64_t vocab, ls_dtype dtype) {
+  const int pol = g_lp_write_policy.load(std::memory_order_relaxed);
+  if (pol != 0) return pol > 0;
   const int64_t l2 = l2_bytes();
+  const int sms = sm_count();
   const int64_t bytes = (int64_t)n * vocab * (dtype == LS_DTYPE_BF16 ? 2 : 4);
-  return l2 > 0 && bytes * 5 <= l2 * 3;
+  return l2 > 0 && sms > 0 && (int64_t)n * 4 <= (int64_t)sms * 3 && vocab >= 16384 && bytes * 5 <= l2 * 3;
 }
 
 // A workspace is absent, or large enough and 16-byte aligned.
@@ -227,6 +240,12 @@ ls_status ls_sample_log_probs(const void* logits, ls_dtype dtype, int64_t logits
   const ls_status rc = dispatch<MODE_BOTH>(a, dtype, route, n, st);
   if (rc != LS_OK || !a.lp_rows) return rc;
   return dispatch_lp_write(a, dtype, n, st);
+}
+
+int ls_set_log_prob_write_policy(int policy) {
+  if (policy != 0 && policy != 1 && policy != -1) return (int)LS_ERR_INVALID_ARG;
+  g_lp_write_policy.store(policy, std::memory_order_relaxed);
+  return (int)LS_OK;
 }
 
 int ls_set_split_policy(int ctas_per_row) {

@@ -42,11 +42,15 @@ def split_policy(request):
     ls.set_split_policy(0)
 
 
-@pytest.fixture(params=[True, False], ids=["tiled-write", "row-write"])
+@pytest.fixture(params=[1, -1, 0], ids=["tiled-write", "row-write", "no-workspace"])
 def lp_write(request):
-    """Log-prob calls with a workspace (rows whose logits fit in L2 are written
-    by the tiled write kernel) and without (the row kernel writes each row)."""
+    """Log-prob calls with a workspace and the tiled write kernel forced, with
+    a workspace and the row kernel's write forced, and without a workspace."""
+    import logits_sampling_gb300 as ls
     from logits_sampling_gb300 import _binding
-    _binding.LOG_PROBS_WORKSPACE = request.param
+    ls.load_library()
+    ls.set_log_prob_write_policy(request.param if request.param != 0 else -1)
+    _binding.LOG_PROBS_WORKSPACE = request.param != 0
     yield request.param
+    ls.set_log_prob_write_policy(0)
     _binding.LOG_PROBS_WORKSPACE = True

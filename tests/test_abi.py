@@ -49,6 +49,15 @@ def test_split_policy_values(lib):
         assert lib.ls_set_split_policy(good) == 0, good
 
 
+def test_log_prob_write_policy_values(lib):
+    """ls_set_log_prob_write_policy accepts 0, 1, -1 and rejects anything else
+    on the host (no GPU needed)."""
+    for bad in (2, -2, 8):
+        assert lib.ls_set_log_prob_write_policy(bad) == 1, bad
+    for good in (1, -1, 0):
+        assert lib.ls_set_log_prob_write_policy(good) == 0, good
+
+
 def test_no_torch_in_the_abi():
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()

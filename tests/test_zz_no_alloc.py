@@ -21,6 +21,9 @@ def _lib():
     import logits_sampling_gb300 as ls
     ls.load_library()
     ls.set_split_policy(0)
+    ls.set_log_prob_write_policy(1)  # the tiled write, which uses the scratch, on every batch
+    yield
+    ls.set_log_prob_write_policy(0)
 
 
 def _both(w, x, step):
