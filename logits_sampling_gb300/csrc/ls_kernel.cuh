@@ -922,7 +922,7 @@ __device__ __forceinline__ void write_group(const RowView<TIn>& rv, float* out, 
 // entries go four at a time: a warp's loads and 16-byte streaming stores
 // cover consecutive addresses (kWriteQuads quads of a thread in flight
 // together); otherwise group by group with the streaming pass's 256-bit loads.
-constexpr int kWriteQuads = 4;
+constexpr int kWriteQuads = 8;
 template <typename TIn, typename KeptF, typename ValF>
 __device__ __forceinline__ void write_row(const RowView<TIn>& rv, float* out, KeptF kept, ValF val) {
   using RVT = RowView<TIn>;
