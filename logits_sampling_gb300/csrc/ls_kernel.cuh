@@ -1140,11 +1140,22 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     float gj = kNegInf;
     if (k_on && (tid >> 5) < wact && k <= 32 * wact) {
       const int jrank = (k + wact - 1) / wact;
-      float cur = m;
-      for (int t = 0; t < jrank; ++t) {
-        gj = warp_max(cur);
-        const unsigned holders = __ballot_sync(0xFFFFFFFFu, cur == gj);
-        if (lane == __ffs(holders) - 1) cur = kNegInf;
+      if (jrank <= 8) {  // a few dependent extractions of the warp maximum
+        float cur = m;
+        for (int t = 0; t < jrank; ++t) {
+          gj = warp_max(cur);
+          const unsigned holders = __ballot_sync(0xFFFFFFFFu, cur == gj);
+          if (lane == __ffs(holders) - 1) cur = kNegInf;
+        }
+      } else {  // each lane's rank among the 32 (ties by lane), all shuffles independent
+        int rank = 0;
+#pragma unroll
+        for (int l = 0; l < 32; ++l) {
+          const float o = __shfl_sync(0xFFFFFFFFu, m, l);
+          rank += (o > m || (o == m && l < lane)) ? 1 : 0;
+        }
+        const unsigned at = __ballot_sync(0xFFFFFFFFu, rank == jrank - 1);
+        gj = __shfl_sync(0xFFFFFFFFu, m, __ffs(at) - 1);
       }
     }
     if (lane == 0) {
