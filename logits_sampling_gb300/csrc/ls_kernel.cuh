@@ -757,6 +757,38 @@ __device__ SelResult radix_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo
   return SelResult{klo, above + mass_at, false};
 }
 
+// Top-p cut whose first level was binned by value (bin_of_key(k): the bin of
+// the entries with key k, non-decreasing in k) rather than by key range: the
+// first level's cut bin, then radix_select over exactly that bin's keys (the
+// keys k in [klo1, khi1] with bin_of_key(k) == b, found by bisection on the
+// monotone bin function).  Same semantics as radix_select over [klo1, khi1].
+template <typename TIn, typename BinOfKey>
+__device__ SelResult value_binned_select(Shared& sh, const Cands<TIn>& cs, uint32_t klo1, uint32_t khi1,
+                                         unsigned long long target, float R, float c, BinOfKey bin_of_key) {
+  unsigned long long tg = target;
+  const unsigned long long total = find_cut_bin(sh, kBins, 0ull, tg, -1.f, BinWeight<TIn>{&sh, BIN_MASS, klo1, c, R});
+  const int b = sh.cut_bin;
+  if (b < 0) return SelResult{klo1, total, true};
+  const unsigned long long above = sh.cut_above, mass_b = sh.cut_mass;
+  // smallest key in [klo1, khi1] whose bin is >= bb (khi1 + 1 if none)
+  auto first_key = [&](int bb) {
+    uint64_t lo = klo1, hi = (uint64_t)khi1 + 1u;
+    while (lo < hi) {
+      const uint64_t mid = lo + (hi - lo) / 2u;
+      if (bin_of_key((uint32_t)mid) >= bb)
+        hi = mid;
+      else
+        lo = mid + 1u;
+    }
+    return lo;
+  };
+  const uint32_t klo = (uint32_t)first_key(b);
+  const uint32_t khi = b + 1 < kBins ? (uint32_t)(first_key(b + 1) - 1u) : khi1;
+  __syncthreads();  // every thread has read the cut fields before the next level rewrites them
+  if (klo >= khi) return SelResult{klo, above + mass_b, false};  // the bin holds one key
+  return radix_select<TIn>(sh, cs, klo, khi, target, -1.f, R, c, above, true, false);
+}
+
 // Exact cuts over a short candidate list (at most kSmallList entries, all of
 // them listed) by direct counting: for each entry x, the number and the
 // fixed-point mass of the listed entries strictly above it.  x survives the
@@ -1260,6 +1292,15 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   const int shift1 = bits1 > kBinBits ? bits1 - kBinBits : 0;
   // first select level, built while collecting (the binning radix_select uses)
   const int mode1 = kind == 1 ? BIN_COUNT : shift1 == 0 ? BIN_KEY_COUNT : BIN_MASS;
+  // A top-p cut over a wide key range bins that first level by value, linearly
+  // over [lc, M]: key-range bins put a flat bf16 row's thousands of candidates
+  // into a few dozen of the 2048 bins, and their mass atomics serialised.
+  const float vscale = (float)kBins / (M - lc);
+  const bool vbin = kind == 2 && mode1 == BIN_MASS && vscale <= FLT_MAX;
+  auto value_bin = [&](float v) {
+    const float t = (v - lc) * vscale;
+    return t <= 0.f ? 0 : t >= (float)(kBins - 1) ? kBins - 1 : (int)t;
+  };
   // sampling rows score the maximum's ties while collecting
   const bool ties_in_take = kSample && !tie_only;
 
@@ -1289,7 +1330,9 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
       ++at;
       if (kind != 0) {
         const uint32_t kk = K::key(x);
-        if (kk >= klo1 && kk <= key_max) {
+        if (vbin) {
+          add_mass(&sh.hist[2 * value_bin(x)], mass_fixed(ex2(fmaf(x, c, -R))));
+        } else if (kk >= klo1 && kk <= key_max) {
           const int bin = (int)((kk - klo1) >> shift1);
           if (mode1 == BIN_MASS)
             add_mass(&sh.hist[2 * bin], mass_fixed(ex2(fmaf(x, c, -R))));
@@ -1445,8 +1488,11 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     // the first level's histogram was built while collecting
     const unsigned long long target =
         kind == 1 ? (unsigned long long)k : max(1ull, __float2ull_ru(fmaxf(p, 0.f) * S * kMassScale));
-    SelResult r1 = small ? small_select<TIn>(sh, cs, klo1, k_on, p_on, k, fmaxf(p, 0.f), target, R, c)
-                         : radix_select<TIn>(sh, cs, klo1, key_max, target, -1.f, R, c, 0ull, kind == 2, true);
+    SelResult r1 =
+        small  ? small_select<TIn>(sh, cs, klo1, k_on, p_on, k, fmaxf(p, 0.f), target, R, c)
+        : vbin ? value_binned_select<TIn>(sh, cs, klo1, key_max, target, R, c,
+                                          [&](uint32_t kk) { return value_bin(K::value(kk)); })
+               : radix_select<TIn>(sh, cs, klo1, key_max, target, -1.f, R, c, 0ull, kind == 2, true);
     if (kind == 2 && r1.short_total && lc > -FLT_MAX) {
       // The candidates weigh less than the top-p target, so the cut lies
       // below the bound: select again over every finite entry, visiting the

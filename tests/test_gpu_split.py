@@ -110,3 +110,21 @@ def test_topp_probe_rounds(policy, dt):
     ids, err, _ = gpu_sample(w)
     assert err == 0
     check_ids(ids, ref, f"probe {dt} split {policy}")
+
+
+@pytest.mark.parametrize("dt", [W.BF16, W.F32])
+def test_topp_flat_rows_row_kernel_log_probs(dt):
+    """The same flat top-p rows through the one-CTA row kernel: its first
+    select level bins values over [lc, M] (a key-range binning put thousands of
+    candidates into a few bins) -- ids and log-prob rows against the oracle."""
+    import logits_sampling_gb300 as ls
+    from gpu_util import check_log_probs, gpu_log_probs
+    ls.set_split_policy(-1)
+    w, ref = _probe_case(dt)
+    ids, err, _ = gpu_sample(w)
+    assert err == 0
+    check_ids(ids, ref, f"flat {dt} row kernel")
+    lp, err = gpu_log_probs(w)
+    assert err == 0
+    rlp = oracle.log_probs(w.logits, 1 if dt == W.BF16 else 0, w.n, w.temperature, w.top_k, w.top_p)
+    check_log_probs(lp, rlp, f"flat {dt} row kernel lp")
