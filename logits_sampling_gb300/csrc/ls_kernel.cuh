@@ -140,15 +140,17 @@ __device__ __forceinline__ unsigned long long read_mass(const unsigned int* pair
 // round(w * 2^40) for a weight w in [0, 1], from the float's bits with integer
 // operations only (64-bit float/integer conversions run on the slow FP64
 // pipe).  Weights below 2^-41 give 0.
+// Branch-free: a right shift by r >= 25 (weights below 2^-40 and the clamp
+// at 63) leaves 0, since mant + 2^(r-1) < 2^r.
 __device__ __forceinline__ unsigned long long mass_fixed(float w) {
   const uint32_t b = __float_as_uint(w);
   const int e = (int)((b >> 23) & 0xFFu);
-  if (e == 0) return 0ull;
   const unsigned long long mant = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
   const int sh = e - 110;  // w * 2^40 = mant * 2^(e - 127 - 23 + 40)
-  if (sh >= 0) return mant << sh;
-  if (sh <= -25) return 0ull;
-  return (mant + (1ull << (-sh - 1))) >> (-sh);
+  const int r = min(max(-sh, 0), 63);
+  const unsigned long long up = mant << min(max(sh, 0), 63);
+  const unsigned long long dn = (mant + ((1ull << r) >> 1)) >> r;
+  return e == 0 ? 0ull : sh >= 0 ? up : dn;
 }
 
 // ---------------------------------------------------------------------------
@@ -613,17 +615,23 @@ __device__ void gumbel_argmax(Shared& sh, const Cands<TIn>& cs, float M, float l
 // the bin has the same value.
 enum BinMode { BIN_COUNT = 0, BIN_MASS = 1, BIN_KEY_COUNT = 2 };
 
+// load() reads a bin's words, weight() turns them into its weight: a level
+// issues every load of a thread before the first weight.
 template <typename TIn>
 struct BinWeight {
   const Shared* sh;
   int mode;
   uint32_t klo;  // key of bin 0 (BIN_KEY_COUNT)
   float c, R;
-  __device__ __forceinline__ unsigned long long operator()(int b) const {
-    if (mode == BIN_MASS) return read_mass(&sh->hist[2 * b]);
-    const unsigned int n = sh->hist[b];
-    if (mode == BIN_COUNT || n == 0u) return n;
-    return (unsigned long long)n * mass_fixed(ex2(fmaf(KeyOps<TIn>::value(klo + (uint32_t)b), c, -R)));
+  __device__ __forceinline__ void load(int b, unsigned int& lo, unsigned int& hi) const {
+    const bool pair = mode == BIN_MASS;
+    lo = sh->hist[pair ? 2 * b : b];
+    hi = pair ? sh->hist[2 * b + 1] : 0u;
+  }
+  __device__ __forceinline__ unsigned long long weight(int b, unsigned int lo, unsigned int hi) const {
+    if (mode == BIN_MASS) return ((unsigned long long)hi << 32) | lo;
+    if (mode == BIN_COUNT) return lo;
+    return (unsigned long long)lo * mass_fixed(ex2(fmaf(KeyOps<TIn>::value(klo + (uint32_t)b), c, -R)));
   }
 };
 
@@ -645,9 +653,12 @@ __device__ __forceinline__ unsigned long long find_cut_bin(Shared& sh, int nb, u
   const bool has_bins = nb - 1 - warp * 32 * kBinsPerThread >= 0;
   unsigned long long w[kBinsPerThread], local = 0, incl = 0;
   if (has_bins) {
+    unsigned int lo[kBinsPerThread], hi[kBinsPerThread];
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) weight.load(max(top - q, 0), lo[q], hi[q]);
 #pragma unroll
     for (int q = 0; q < kBinsPerThread; ++q) {
-      w[q] = top - q >= 0 ? weight(top - q) : 0ull;
+      w[q] = top - q >= 0 ? weight.weight(top - q, lo[q], hi[q]) : 0ull;
       local += w[q];
     }
     incl = local;
@@ -1397,11 +1408,17 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
     const int nslots = (rv.NG + kThreads - 1) / kThreads;
     for (int sb = 0; sb < nslots; sb += 32) {
       const int send = min(32, nslots - sb);
+      // eight maxima in flight (indices clamped into the row), then the tests
       uint32_t mask = 0u;
-#pragma unroll 8
-      for (int q = 0; q < send; ++q) {
-        const int g = tid + (sb + q) * kThreads;
-        if (g < rv.NG && gmax[g] >= lc) mask |= 1u << q;
+      for (int q0 = 0; q0 < send; q0 += 8) {
+        float gm[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) gm[u] = gmax[min(tid + (sb + q0 + u) * kThreads, rv.NG - 1)];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int g = tid + (sb + q0 + u) * kThreads;
+          mask |= (g < rv.NG && gm[u] >= lc ? 1u : 0u) << (q0 + u);
+        }
       }
       const int cnt = __popc(mask);
       int incl = cnt;
