@@ -1453,8 +1453,26 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // next read after the cut's barriers); only more than kTieList ties take a
   // pass over the list.
   const uint64_t step = sh.step;
+  // A sampling row whose whole list fits one entry per thread scores every
+  // candidate here, the last threads first (the first warps hold the cut's
+  // bins): the kept set lies in the list, and an entry that can never win
+  // (below the noise bound) may be scored too.  The ties' scores go to
+  // sh.best at once, as below; after the cut the best kept score is a warp
+  // maximum and one atomic per warp instead of a Gumbel pass.
+  const bool pre = kSample && !tie_only && cs.listed && count <= kThreads;
+  const int pe = kThreads - 1 - tid;  // this thread's entry
+  float pv = kNegInf;
+  unsigned long long pkey = 0ull;
+  if (pre && pe < count) {
+    pv = cand_v[pe];
+    const int64_t j = cand_j[pe];
+    pkey = argmax_key(__fdiv_rn(pv, T) + gumbel_of_word(noise_word(seed, step, (uint32_t)i, j)), j);
+    if (pv >= M) atomicMax(&sh.best, pkey);
+  }
   const int nties = ties_in_take && lc <= M ? sh.tie_count : -1;
-  if (nties >= 0 && nties <= kTieList) {
+  if (pre) {
+    // the ties were scored with the list
+  } else if (nties >= 0 && nties <= kTieList) {
     const int q = kThreads - 1 - tid;
     if (q < nties) score_entry(&sh.best, M, T, seed, step, (uint32_t)i, sh.tie_j[q]);
   } else if (tie_only || kSample) {
@@ -1531,7 +1549,18 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
 
   if (kSample) {
     // ---- Gumbel-max over the kept set ------------------------------------
-    gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, seed, step, (uint32_t)i);
+    if (pre && cs.listed) {
+      unsigned long long kk = pv >= lo_val ? pkey : 0ull;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long u = __shfl_xor_sync(0xFFFFFFFFu, kk, o);
+        kk = u > kk ? u : kk;
+      }
+      if (lane == 0 && kk != 0ull) atomicMax(&sh.best, kk);
+      __syncthreads();
+    } else {
+      gumbel_argmax(sh, cs, M, fmaxf(lo_val, lg), T, seed, step, (uint32_t)i);
+    }
     if (tid == 0) {
       const int32_t id = argmax_index(sh.best);
       a.out_ids[i] = id;
