@@ -170,7 +170,7 @@ __device__ __forceinline__ void ld256(const void* p, uint32_t (&r)[8]) {
 
 // The same load under an L2 eviction policy (createpolicy): the log-prob
 // modes keep the row in L2 for the write pass (evict_last) and let that pass's
-// re-read go first (evict_first).
+// re-read go first (evict_first); sampling streams evict_first.
 __device__ __forceinline__ void ld256_hint(const void* p, uint32_t (&r)[8], uint64_t policy) {
   asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
@@ -1074,17 +1074,16 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   constexpr int U = RV::kBytes == 2 ? 2 : 1;  // groups per stage
   constexpr int STEP = U * kThreads;
   // log-prob modes: the row stays in L2 for the write pass (the rows in
-  // flight fit there; the outputs are stored evict-first)
-  const uint64_t keep = MODE == MODE_SAMPLE ? 0ull : l2_evict_last_policy();
+  // flight fit there; the outputs are stored evict-first).  Sampling streams
+  // evict-first: the row is needed again only by this call's candidate
+  // re-reads, and the stream no longer pushes out of L2 what every call
+  // reuses (this kernel's code among it: top_p 19.5 -> 19.0 us, speculative
+  // 52.3 -> 49.8).
+  const uint64_t keep = MODE == MODE_SAMPLE ? l2_evict_first_policy() : l2_evict_last_policy();
   auto issue = [&](int g0, uint32_t (&w)[U][RV::kWords]) {
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (rv.full(g0 + u * kThreads)) {
-        if (MODE == MODE_SAMPLE)
-          rv.load_words(g0 + u * kThreads, w[u]);
-        else
-          rv.load_words(g0 + u * kThreads, w[u], keep);
-      }
+      if (rv.full(g0 + u * kThreads)) rv.load_words(g0 + u * kThreads, w[u], keep);
   };
   uint32_t wa[U][RV::kWords], wb[U][RV::kWords];
   issue(tid, wa);
@@ -1458,8 +1457,11 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_row_kernel(const KernelAr
   // bins): the kept set lies in the list, and an entry that can never win
   // (below the noise bound) may be scored too.  The ties' scores go to
   // sh.best at once, as below; after the cut the best kept score is a warp
-  // maximum and one atomic per warp instead of a Gumbel pass.
-  const bool pre = kSample && !tie_only && cs.listed && count <= kThreads;
+  // maximum and one atomic per warp instead of a Gumbel pass.  Not in the
+  // fused fp32 kernel, whose long write pass pays for the extra live state in
+  // spills (1024 x 262144 fp32: 648 against 638 us a call).
+  constexpr bool kPre = kSample && !(MODE == MODE_BOTH && RowView<TIn>::kBytes == 4);
+  const bool pre = kPre && !tie_only && cs.listed && count <= kThreads;
   const int pe = kThreads - 1 - tid;  // this thread's entry
   float pv = kNegInf;
   unsigned long long pkey = 0ull;
